@@ -1,0 +1,460 @@
+"""Benchmark of the fused ZeRO update step on one GB300 (or N independent replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload flat1b_n8] [--api plan|step] [--in-place]
+
+One step is one pass of the whole hot path over one batch of synthetic
+gradients, resident in device memory when the timed region starts:
+  - reduce-scatter of the N ranks' gradients with 1/N batch-mean scaling and
+    loss-scale removal;
+  - the overflow check and the global norm;
+  - owner-local Adam on the FP32 master/m/v;
+  - the BF16 cast and all-gather into the full working-weight view;
+  - the host bookkeeping (step counter, dynamic loss scale).
+The default workload is flat1b_n8: 1,000,000,000 parameters, N=8 BF16 ranks,
+25,000,000-element buckets, dynamic loss scale from 65536, skip on overflow.
+It runs out of place (zero_step_into), so the skip decision needs no second
+pass.
+
+The printed JSON line carries:
+  - value: params/s over all GPUs;
+  - the dominant kernel's roofline: algorithmic bytes per launch over its
+    CUDA-event duration, against the measured HBM copy peak;
+  - the oracle timed on host cores (cpu_baseline);
+  - an end-to-end figure: gradients streamed from pinned host memory through
+    two device slots, and the result read back to the host;
+  - the SM clocks sampled during the timed region, and the count of this
+    library's kernel launches.
+Under torchrun each rank runs an independent replica on its own GPU ("replicas
+only": the in-device step has no cross-GPU exchange); a gloo group carries
+only the barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "params/sec and achieved HBM GB/s (fraction of GB300 peak) per fused ZeRO step"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_04_gb300", "csrc", "zero_step.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "zero_fused_kernel_flat1b_n8.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flat1b_n8")
+    ap.add_argument("--api", choices=["plan", "step"], default="plan")
+    ap.add_argument("--in-place", action="store_true",
+                    help="zero_step in place (two passes when skipping) instead of zero_step_into")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 10)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Group:
+    """Barrier and max over ranks on a gloo group (control plane only)."""
+
+    def __init__(self, world: int):
+        self.world = world
+        if world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t[0])
+
+    def sum(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.SUM)
+        return float(t[0])
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+CLOCK_FIELDS = ["uuid", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons every 100 ms."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(CLOCK_FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(CLOCK_FIELDS):
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows]
+        reasons = sorted({REASONS[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(num(r[3]) for r in rows)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def read_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic_per_param() -> float | None:
+    """DRAM bytes per parameter of the fused kernel from the committed ncu
+    summary, if it was taken on the kernel source as it is now."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    b = re.search(r"traffic_bytes_per_param:\s*([0-9.]+)", text)
+    if not h or not b or h.group(1) != kernel_source_hash():
+        return None
+    return float(b.group(1))
+
+
+def alg_bytes_per_param(wl) -> int:
+    """N*g grad reads + 12 state reads + 12 state writes + 2 weight writes."""
+    return wl.N * wl.grad_bytes + 26
+
+
+def cpu_baseline(oracle, wl, grads, master, budget_s: float, max_elems: int) -> dict:
+    """The oracle, single-threaded, on the first elements of the same
+    gradients and master weights (copied from the device), stepped until
+    ``budget_s`` of CPU time is used."""
+    import numpy as np
+    from zero_sharded_mixed_04_gb300 import synth
+    n = min(max_elems, wl.psi_pad) // (wl.N * 128) * (wl.N * 128)
+    g = [synth.to_numpy_grad(x[:n]) for x in grads]
+    p = master[:n].cpu().numpy().copy()
+    m, v, w = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+    hp = oracle.Hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                        weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm)
+    steps, t0 = 0, time.process_time()
+    w0 = time.perf_counter()
+    while True:
+        oracle.zero_step(g, p, m, v, w, hp, steps + 1, wl.loss_scale, wl.skip_on_overflow)
+        steps += 1
+        if time.process_time() - t0 >= budget_s:
+            break
+    wall = time.perf_counter() - w0
+    return {"value": steps * n / wall, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} oracle step(s) of {wl.name} on its first {n} parameters "
+                      f"(all {wl.N} ranks), single-threaded C, {wall:.1f} s wall"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+    from zero_sharded_mixed_04_gb300 import build
+    build.build_library()
+    from zero_sharded_mixed_04_gb300 import synth
+    from zero_sharded_mixed_04_gb300 import zero as Z
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+
+    group = Group(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    out_of_place = not args.in_place
+    grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
+    master = synth.make_master(wl, dev)
+    opt = ZeroAdam(wl.psi_pad, wl.N, wl.grad_dtype, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                   eps=wl.eps, weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm,
+                   skip_on_overflow=wl.skip_on_overflow, bucket_elems=wl.bucket_elems,
+                   loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
+                   out_of_place=out_of_place, device=dev, master=master)
+    buckets = opt.bucket_bounds()
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in buckets]
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(timed_launches: list | None):
+        ev = events if (args.api == "plan" and timed_launches is not None) else None
+        opt.enqueue(grads, stream, api=args.api, bucket_events=ev)
+        res = opt.finish(stream)
+        if not res["applied"]:
+            raise RuntimeError("benchmark step was skipped: the synthetic gradients overflowed")
+        if ev is not None:
+            timed_launches.extend(a.elapsed_time(b) for a, b in ev)
+
+    for _ in range(args.warmup):
+        one_step(None)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    launch_ms: list[float] = []
+    group.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = Z.zero_launch_count()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        one_step(launch_ms)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    group.barrier()
+    launches = Z.zero_launch_count() - launches0
+    clock_info = clocks.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms_max = group.max(ms)
+    params_total = group.sum(float(wl.psi))
+    value = params_total / (ms_max / 1e3)
+
+    peak, peak_kind = read_peaks()
+    b_alg = alg_bytes_per_param(wl)
+    roofline = None
+    if launch_ms:
+        per_step_kernel_ms = sum(launch_ms) / args.steps
+        achieved = b_alg * wl.psi_pad / (per_step_kernel_ms / 1e3) / 1e9
+        tpp = profiled_traffic_per_param()
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4),
+                    "traffic": (None if tpp is None else round(tpp * wl.psi_pad / len(buckets))),
+                    "peak_kind": peak_kind,
+                    "kernel": "zero_fused_kernel" if opt.hp.max_grad_norm == 0 and out_of_place
+                    else "zero_reduce_kernel",
+                    "launches_per_step": len(buckets),
+                    "avg_launch_ms": round(per_step_kernel_ms / len(buckets), 5),
+                    "alg_bytes_per_param": b_alg}
+    step_gbs = b_alg * wl.psi_pad / (ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, opt, grads, wl, stream, dev, group)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cpu = cpu_baseline(oracle, wl, grads, opt.state()["master"], budget_s=10.0,
+                           max_elems=1 << 24)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "psi": wl.psi, "psi_pad": wl.psi_pad, "N": wl.N,
+                   "grad_dtype": wl.grad_dtype, "bucket_elems": wl.bucket_elems,
+                   "loss_scale": wl.loss_scale, "dynamic_loss_scale": wl.dynamic_loss_scale,
+                   "skip_on_overflow": wl.skip_on_overflow, "max_grad_norm": wl.max_grad_norm,
+                   "entry": ("zero_plan_* (= zero_step_into)" if args.api == "plan"
+                             else "zero_step_into") if out_of_place else
+                   ("zero_plan_* (= zero_step)" if args.api == "plan" else "zero_step"),
+                   "l2": "inputs larger than L2: %.1f GB moved per step" %
+                         (b_alg * wl.psi_pad / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, N ranks in HBM"},
+        "achieved_hbm_gbs": round(step_gbs, 1),
+        "hbm_frac": round(step_gbs / peak, 4),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clock_info,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    group.close()
+
+
+def run_e2e(args, opt, grads, wl, stream, dev, group) -> dict:
+    """The same step through the public API with the gradients in pinned host
+    memory: every step copies them host-to-device through two bucket slots
+    (overlapped with the reduction of the previous bucket) and reads the
+    step result back to the host."""
+    import torch
+    # one pinned allocation for all ranks (the pinned allocator rounds each
+    # allocation up to a power of two)
+    n = grads[0].numel()
+    flat = torch.empty(n * len(grads), dtype=grads[0].dtype, pin_memory=True)
+    host = [flat[i * n:(i + 1) * n] for i in range(len(grads))]
+    for h, g in zip(host, grads):
+        h.copy_(g)
+    slots = opt.make_slots()
+    copy_stream = torch.cuda.Stream(dev)
+    steps = args.e2e_steps or max(1, min(args.steps, 10))
+    opt.enqueue_from_host(host, slots, copy_stream, stream)  # one untimed warm-up step
+    opt.finish(stream)
+    group.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        opt.enqueue_from_host(host, slots, copy_stream, stream)
+        res = opt.finish(stream)  # the step result, read on the host
+        if not res["applied"]:
+            raise RuntimeError("e2e step was skipped")
+    torch.cuda.synchronize(dev)
+    dt = (time.perf_counter() - t0) / steps
+    dt = group.max(dt)
+    h2d = sum(g.numel() * g.element_size() for g in grads)
+    del host, slots, flat
+    return {"value": round(group.sum(float(wl.psi)) / dt, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16, "ms_per_step": round(dt * 1e3, 3),
+            "path": "pinned host grads -> two device bucket slots -> zero_plan_bucket; "
+                    "result read by the host"}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    from zero_sharded_mixed_04_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    oracle.build()
+    unit = wl.N * 128
+    # size each step's sample so the whole run takes about a minute
+    calib_n = 1 << 18
+    hp = oracle.Hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                        weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm)
+
+    def sample(n):
+        grads = synth.make_grads(wl, 1, "cpu", psi=n, psi_pad=n)
+        g = [synth.to_numpy_grad(x) for x in grads]
+        p = synth.make_master(wl, "cpu", psi_pad=n, psi=n).numpy()
+        return g, p, np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+
+    g, p, m, v, w = sample(calib_n)
+    t0 = time.perf_counter()
+    oracle.zero_step(g, p, m, v, w, hp, 1, wl.loss_scale, wl.skip_on_overflow)
+    ns = (time.perf_counter() - t0) / calib_n * 1e9
+    n = int(60.0 / (args.steps + args.warmup) / (ns * 1e-9))
+    n = max(unit, min(1 << 25, n // unit * unit))
+    g, p, m, v, w = sample(n)
+    for k in range(args.warmup):
+        oracle.zero_step(g, p, m, v, w, hp, k + 1, wl.loss_scale, wl.skip_on_overflow)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        oracle.zero_step(g, p, m, v, w, hp, args.warmup + k + 1, wl.loss_scale,
+                         wl.skip_on_overflow)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n / dt
+    desc = (f"each step: one oracle step of {wl.name} on a {n}-parameter sample (all {wl.N} "
+            f"ranks), single-threaded C on the host")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "psi": wl.psi, "N": wl.N, "grad_dtype": wl.grad_dtype,
+                   "sample_params": n},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

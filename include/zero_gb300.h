@@ -1,0 +1,314 @@
+/*
+ * zero_gb300.h -- C ABI of libzero_gb300.so, the GB300 (sm_103a) ZeRO
+ * sharded mixed-precision update step.
+ *
+ * What one step computes.  N data-parallel ranks each hold a gradient buffer
+ * for the same flat parameter vector.
+ *   1. Reduce-scatter.  Each element's N contributions are added in rank order
+ *      0..N-1 in FP32, starting from +0.  The sum is scaled by
+ *      fp32(1 / (N * loss_scale)) to the batch mean.
+ *   2. Owner update.  Each owner r updates its own slice of the FP32 master
+ *      weights and Adam moments m and v with the combined gradient.
+ *   3. All-gather.  The updated master is rounded to BF16 (nearest, ties to
+ *      even) and written into the one full working-weight view.
+ * The N ranks are simulated inside one GPU: the N gradient buffers and the N
+ * owners' slices all live in this device's memory, so the collectives are
+ * in-device data movement.  Nothing crosses to another GPU.
+ *
+ * Sources (web pages; section names as printed there):
+ *   - lecture deck "RC-T2: sharing data and sharing the duty to store are two
+ *     different acts", note N48.  Reduce-scatter adds the contributions of the
+ *     same parameter only, scales them to match a batch-mean loss and hands
+ *     the result to the slice's owner.  The owner updates with its own master
+ *     and m/v.  The next all-gather fetches the updated parameters.
+ *   - topic page "Putting the training ledger onto multiple devices",
+ *     section "one full ZeRO-3 computation".  Defines all-gather,
+ *     reduce-scatter and all-reduce as data semantics, all-reduce being
+ *     reduce-scatter followed by all-gather.
+ *   - blog post "Data parallelism and ZeRO: how much each of the three stages
+ *     saves".  Section "16 bytes per parameter" gives the per-parameter ledger
+ *     2 + 2 + 4 + 4 + 4 B.  Section "three stages" and its table cover ZeRO-1/2:
+ *     reduce-scatter, an owner step on 1/N of the FP32 state, then an
+ *     all-gather of the BF16 weights.  They also give the bytes per parameter
+ *     and the communication volume of each stage.
+ *   Where the pages say nothing, this library uses these readings:
+ *   - Adam with bias correction; eps is added after sqrt(v_hat).
+ *   - AdamW's decoupled weight decay, applied to the master weight first.
+ *   - The overflow check runs on the scaled FP32 combined gradient.
+ *   - The clip coefficient is min(1, max_norm / (norm + 1e-6)).
+ *
+ * Layout.  The flat vector holds psi parameters, zero-padded to psi_pad, a
+ * multiple of N * ZERO_PAD_UNIT.  Owner r holds the contiguous slice
+ * [r*S, (r+1)*S), with S = psi_pad / N.
+ *
+ * Ownership.  The caller allocates and frees every device buffer: the N
+ * gradient buffers, master/m/v, the BF16 working weights and the workspace.
+ * The step entry points allocate nothing and keep no hidden state between
+ * calls.
+ *
+ * Errors.  Argument errors are detected on the host before any work is
+ * enqueued.  The function returns a negative zero_status and modifies
+ * nothing.  A CUDA error raised while enqueueing returns ZERO_ERR_CUDA.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_PAD_UNIT 128      /* psi_pad is a multiple of N * ZERO_PAD_UNIT   */
+#define ZERO_MAX_RANKS 64      /* largest N accepted                           */
+#define ZERO_ALIGN_BYTES 16    /* every buffer must start on this boundary     */
+#define ZERO_BUCKET_ALIGN 8    /* bucket_elems must be a multiple of this      */
+
+typedef enum {
+    ZERO_OK = 0,              /* success; for a step: the update was applied       */
+    ZERO_STEP_SKIPPED = 1,    /* the step found a non-finite gradient and skipped  */
+    ZERO_ERR_ARG = -1,        /* bad size, count, pointer or hyper-parameter       */
+    ZERO_ERR_ALIGN = -2,      /* a buffer not on a ZERO_ALIGN_BYTES boundary       */
+    ZERO_ERR_CUDA = -3,       /* a CUDA call failed while enqueueing               */
+    ZERO_ERR_TIMEOUT = -4,    /* a bounded wait inside a kernel gave up            */
+    ZERO_ERR_WORKSPACE = -5,  /* workspace missing, too small or misaligned        */
+    ZERO_ERR_OVERLAP = -6     /* two buffers that must be disjoint overlap         */
+} zero_status;
+
+typedef enum {
+    ZERO_GRAD_BF16 = 0,       /* gradients as BF16 (2 B per element) */
+    ZERO_GRAD_FP32 = 1        /* gradients as FP32 (4 B per element) */
+} zero_grad_dtype;
+
+/* The flat layout of a list of tensors (see zero_init_layout). */
+typedef struct {
+    int64_t psi;        /* parameters: the sum of the tensor sizes       */
+    int64_t psi_pad;    /* psi rounded up to a multiple of N * pad_unit  */
+    int64_t shard;      /* S = psi_pad / N, the size of one owner's slice */
+    int64_t n_tensors;
+    int32_t N;          /* data-parallel ranks (the sharding factor)     */
+    int32_t pad_unit;   /* ZERO_PAD_UNIT                                 */
+} zero_layout;
+
+/* Hyper-parameters of one step.  The Adam scalars are FP64, as a host holds
+ * them.  The library rounds each derived scalar once to FP32:
+ *   beta1, 1-beta1, beta2, 1-beta2, eps, lr/(1-beta1^t), sqrt(1-beta2^t), 1-lr*wd. */
+typedef struct {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;      /* decoupled (AdamW); 0 turns it off                */
+    double max_grad_norm;     /* > 0: clip by the global L2 norm; 0: no clipping   */
+    int64_t step;             /* t >= 1: count of applied steps including this one */
+    int32_t skip_on_overflow; /* 1: any non-finite combined gradient skips the step */
+    int32_t reserved;         /* must be 0                                         */
+    int64_t bucket_elems;     /* > 0: walk the flat vector in buckets of this many
+                                 elements (a multiple of ZERO_BUCKET_ALIGN); 0: one
+                                 bucket                                            */
+} zero_adam_hparams;
+
+/* Outcome of one step, written by the device at the end of the step. */
+typedef struct {
+    int32_t status;           /* ZERO_OK (applied), ZERO_STEP_SKIPPED or ZERO_ERR_TIMEOUT */
+    uint32_t found_nonfinite; /* 1 if any combined gradient element was inf or NaN        */
+    float grad_norm;          /* L2 norm of the combined batch-mean gradient, before clip */
+    float clip_coef;          /* factor applied to the gradient (1 without clipping)      */
+} zero_step_result;
+
+/* Flat layout of n_tensors tensors with the given element counts,
+ * concatenated in order with no gaps.  The vector is padded with zeros up to
+ * psi_pad, a multiple of N * ZERO_PAD_UNIT, so that every owner's slice has
+ * the same size S = psi_pad / N.  That is each rank's 1/N share
+ * (RC-T2, slide b1 and note N47; DP-ZeRO blog, "three stages").
+ *   tensor_numel    host array of n_tensors sizes (>= 0); may be NULL if n_tensors == 0
+ *   N               ranks, 1 .. ZERO_MAX_RANKS
+ *   out             host struct, filled on success
+ *   tensor_offsets  host array of n_tensors int64 (caller-owned) that receives
+ *                   each tensor's start in the flat vector; may be NULL
+ * Returns ZERO_OK or ZERO_ERR_ARG (nothing written on error).  Host only. */
+int zero_init_layout(const int64_t* tensor_numel, int64_t n_tensors, int32_t N,
+                     zero_layout* out, int64_t* tensor_offsets);
+
+/* Owner r's slice [*begin, *end) of the flat vector.  Host only.
+ * Returns ZERO_OK or ZERO_ERR_ARG. */
+int zero_shard_range(const zero_layout* layout, int32_t r, int64_t* begin, int64_t* end);
+
+/* Bytes of device workspace a step needs, for the given size and
+ * hyper-parameters.  in_place = 1 is for zero_step and 0 for zero_step_into.
+ * The workspace holds:
+ *   - a 256-byte control block;
+ *   - per-CTA partial sums for the norm;
+ *   - when the step must see the whole gradient before it may update
+ *     anything, an FP32 copy of the combined gradient (psi_pad * 4 bytes).
+ *     This is needed with clipping, and for an in-place step with
+ *     skip_on_overflow.
+ * Returns 0 if the arguments are invalid. */
+size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, int32_t in_place);
+
+/* One ZeRO update step, in place (RC-T2 note N48; DP-ZeRO blog "three stages").
+ *   grads        host array of N device pointers.  grads[i] is rank i's
+ *                gradient for the whole flat vector: psi_pad elements of
+ *                grad_dtype, zero on the padding.  The step only reads them.
+ *   grad_dtype   ZERO_GRAD_BF16 or ZERO_GRAD_FP32
+ *   master, m, v device FP32 arrays of psi_pad elements, updated in place.
+ *                Owner r's slice is [r*S, (r+1)*S).
+ *   w_bf16       device array of psi_pad BF16 values (uint16 bit patterns):
+ *                the full working-weight view that the all-gather fills
+ *   psi_pad, N   sizes; psi_pad must be a multiple of N * ZERO_PAD_UNIT
+ *   hp           host pointer to the hyper-parameters
+ *   loss_scale   > 0; the gradients hold loss_scale times the true gradient
+ *   workspace    device buffer of at least zero_workspace_bytes(psi_pad, hp, 1)
+ *                bytes, 256-byte aligned.  Its contents need no
+ *                initialisation.  Calls that share one workspace must be
+ *                ordered on one stream.
+ *   result       device-accessible zero_step_result (device memory, or pinned
+ *                host memory that the device can address), written when the
+ *                step completes on `stream`; or NULL.  With NULL the call
+ *                waits for the step and returns its status.
+ *   stream       cudaStream_t to enqueue on (NULL = the legacy default stream)
+ * All device buffers must be ZERO_ALIGN_BYTES-aligned.  None may overlap
+ * another: the gradients, master, m, v, w_bf16 and the workspace are checked.
+ * With hp->skip_on_overflow set and a non-finite combined gradient, master,
+ * m, v and w_bf16 are left bit-for-bit unchanged and the status is
+ * ZERO_STEP_SKIPPED.  The step counter and the loss scale are the caller's:
+ * this library never changes them.
+ * Returns ZERO_OK once the step is enqueued (result != NULL), the step's
+ * status (result == NULL), or a negative error code. */
+int zero_step(const void* const* grads, int32_t grad_dtype,
+              float* master, float* m, float* v, uint16_t* w_bf16,
+              int64_t psi_pad, int32_t N, const zero_adam_hparams* hp, float loss_scale,
+              void* workspace, size_t workspace_bytes,
+              zero_step_result* result, void* stream);
+
+/* The same step, out of place.  It reads master/m/v from src_* and writes the
+ * post-step master/m/v and BF16 weights to dst_*.  The caller swaps the two
+ * buffer sets between steps.  With skip_on_overflow set, a skipped step
+ * copies src to dst (src_w_bf16 to dst_w_bf16 included), so dst always holds
+ * the valid post-step state.  Because the old state is never overwritten, the
+ * overflow decision needs no second pass over the gradients.  A step with
+ * skip_on_overflow and no clipping reads each gradient and state element once
+ * and writes each output once.  src_w_bf16 is read only by a skipped step.
+ * Other arguments and errors are as for zero_step.  Every dst buffer must be
+ * disjoint from every src buffer, from the gradients and from the workspace.
+ * The workspace needs zero_workspace_bytes(psi_pad, hp, 0) bytes. */
+int zero_step_into(const void* const* grads, int32_t grad_dtype,
+                   const float* src_master, const float* src_m, const float* src_v,
+                   const uint16_t* src_w_bf16,
+                   float* dst_master, float* dst_m, float* dst_v, uint16_t* dst_w_bf16,
+                   int64_t psi_pad, int32_t N, const zero_adam_hparams* hp, float loss_scale,
+                   void* workspace, size_t workspace_bytes,
+                   zero_step_result* result, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Bucketed form of the same step.
+ *
+ * The ledger page, section "one full ZeRO-3 computation", notes two things.
+ * Real systems group gradients into buckets and synchronise the ready ones
+ * while later layers are still running backward.  The DP-ZeRO blog, section
+ * "offloading the shard to the CPU: two buffers", streams gradient chunks
+ * through two device slots: one in use, one loading.  A plan lets a caller do
+ * either.  It enqueues the reduce-scatter one bucket at a time, in flat order,
+ * each bucket as soon as its gradients are ready.  A bucket's gradients may sit
+ * anywhere, for example in one of two staging slots.  The owner update is
+ * committed at the end, once the step-wide checks are known.
+ *
+ *   zero_plan_init    check and record every argument, as zero_step or
+ *                     zero_step_into would (host only, nothing enqueued)
+ *   zero_plan_begin   reset the step's control block in the workspace
+ *   zero_plan_bucket  enqueue the first pass over [begin, end), the next bucket
+ *   zero_plan_end     enqueue the step-wide decision and the commit, then
+ *                     report the result as zero_step does
+ * zero_step is zero_plan_init, zero_plan_begin, one zero_plan_bucket per
+ * bucket and zero_plan_end.  All calls of one step go to one stream.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    const void* grads[ZERO_MAX_RANKS]; /* rank i's gradient for the whole vector          */
+    const float* src_master;
+    const float* src_m;
+    const float* src_v;
+    const uint16_t* src_w_bf16;
+    float* dst_master;                 /* == src_master for an in-place step              */
+    float* dst_m;
+    float* dst_v;
+    uint16_t* dst_w_bf16;
+    void* workspace;
+    size_t workspace_bytes;
+    int64_t psi_pad;
+    int64_t cursor;                    /* next element a bucket must start at             */
+    zero_adam_hparams hp;
+    float loss_scale;
+    int32_t grad_dtype;
+    int32_t N;
+    int32_t in_place;
+    int32_t two_pass;                  /* 1 if the update waits for a second pass          */
+    int32_t state;                     /* 0 unset, 1 initialised, 2 begun                 */
+} zero_plan;
+
+/* Fills *plan from the arguments of zero_step (dst == src) or zero_step_into
+ * (dst != src), after the same checks; returns their error codes.  grads is
+ * copied, so the caller's array need not outlive the call.  A grads[i] may be
+ * NULL if every bucket will pass its own gradient pointers. */
+int zero_plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
+                   const float* src_master, const float* src_m, const float* src_v,
+                   const uint16_t* src_w_bf16, float* dst_master, float* dst_m, float* dst_v,
+                   uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
+                   const zero_adam_hparams* hp, float loss_scale, void* workspace,
+                   size_t workspace_bytes);
+
+/* Starts the step: clears the control block on `stream`. */
+int zero_plan_begin(zero_plan* plan, void* stream);
+
+/* First pass over elements [begin, end) of the flat vector.  begin must equal
+ * plan->cursor (buckets arrive in flat order, without gaps).  end is a multiple
+ * of ZERO_BUCKET_ALIGN or psi_pad, and begin < end <= psi_pad.
+ *   bucket_grads  NULL to read plan->grads[i] + begin; otherwise a host array of
+ *                 N device pointers.  bucket_grads[i] points at rank i's
+ *                 contribution to element `begin`, and the next end - begin
+ *                 elements follow it: a staging slot, say.  Each must be
+ *                 ZERO_ALIGN_BYTES-aligned and must not overlap a written buffer.
+ * The bucket's gradients are read by the time the stream passes this call, so
+ * the buffer may be refilled after an event recorded right after it. */
+int zero_plan_bucket(zero_plan* plan, int64_t begin, int64_t end,
+                     const void* const* bucket_grads, void* stream);
+
+/* Ends the step once every element has been covered (plan->cursor ==
+ * psi_pad).  It enqueues the step-wide decision and then the commit: the
+ * second pass, or the copy of a skipped out-of-place step.  result and the
+ * return value are as for zero_step. */
+int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream);
+
+/* Persistent bytes one rank holds under a ZeRO stage: 0 = replicated data
+ * parallelism, 1 = optimizer state sharded, 2 = also gradients, 3 = also the
+ * working weights.  A replicated part counts psi elements.  A sharded part
+ * counts ceil(psi / N) elements.  The BF16 working weight is 2 B per
+ * parameter, the gradient grad_bytes (2 or 4) and the optimizer state
+ * optim_bytes (12 for Adam's FP32 master/m/v, 8 with a first moment only).
+ * With grad_bytes = 2 and optim_bytes = 12 this gives 16, 4+12/N, 2+14/N and
+ * 16/N bytes per parameter.  See the DP-ZeRO blog's stage table, and RC-T2
+ * note N47: 128/56/44/32 GB for 8e9 parameters on 4 ranks.  GB there means
+ * 1e9 bytes, counting persistent state only.  Host only.
+ * Returns -1 on a bad argument. */
+int64_t zero_ledger(int64_t psi, int32_t N, int32_t stage, int32_t grad_bytes,
+                    int32_t optim_bytes);
+
+/* Elements each rank sends per step under a stage, counted as the DP-ZeRO
+ * blog's stage table counts them.  Stages 0-2 send 2*psi: one reduce-scatter
+ * and one all-gather, i.e. one all-reduce.  Stage 3 sends 3*psi: one more
+ * all-gather.  The ledger page warns that this multiple depends on the
+ * counting convention.  Host only.  Returns -1 on a bad argument. */
+int64_t zero_comm_volume(int64_t psi, int32_t N, int32_t stage);
+
+/* Static text for a zero_status value. */
+const char* zero_status_str(int status);
+
+/* Number of kernels this library has launched in this process.  Host only,
+ * monotonic, thread-safe.  Memsets and copies are not counted. */
+uint64_t zero_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_H */

@@ -26,3 +26,12 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="session")
+def zero_lib():
+    """The C-ABI binding, building libzero_gb300.so first if it is stale."""
+    from zero_sharded_mixed_04_gb300 import build
+    build.build_library()
+    from zero_sharded_mixed_04_gb300 import zero
+    return zero

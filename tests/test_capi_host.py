@@ -1,0 +1,239 @@
+"""The C-ABI library on the host: it loads, exports every function the header
+declares, and its host-only entry points (layout, ledger, communication
+count, argument checking) agree with the oracle.  No GPU work is launched:
+every zero_step call here fails argument validation before enqueueing."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(zero_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("zero_init_layout", "zero_step", "zero_ledger", "zero_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(zero_lib):
+    lib = ctypes.CDLL(zero_lib.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert sorted(zero_lib.exported_symbols()) == _declared_functions()
+
+
+@pytest.mark.parametrize("numel,N", [([1], 1), ([3, 5, 7], 4), ([128] * 8, 8), ([1000, 24], 3),
+                                     ([], 2), ([50257 * 768, 768, 768], 4), ([5], 64)])
+def test_layout_matches_oracle(zero_lib, oracle_mod, numel, N):
+    rc, lay, offs = zero_lib.zero_init_layout(numel, N)
+    assert rc == zero_lib.ZERO_OK
+    o_offs, psi, psi_pad, shard = oracle_mod.layout(numel, N)
+    assert (lay.psi, lay.psi_pad, lay.shard, lay.N, lay.n_tensors) == (psi, psi_pad, shard, N,
+                                                                        len(numel))
+    assert list(offs) == list(o_offs)
+    for r in range(N):
+        rc, b, e = zero_lib.zero_shard_range(lay, r)
+        assert rc == 0 and (b, e) == (r * shard, (r + 1) * shard)
+    assert zero_lib.zero_shard_range(lay, N)[0] == zero_lib.ZERO_ERR_ARG
+
+
+def test_layout_rejects_bad_arguments(zero_lib):
+    assert zero_lib.zero_init_layout([1, -1], 2)[0] == zero_lib.ZERO_ERR_ARG
+    assert zero_lib.zero_init_layout([1], 0)[0] == zero_lib.ZERO_ERR_ARG
+    assert zero_lib.zero_init_layout([1], 65)[0] == zero_lib.ZERO_ERR_ARG
+
+
+@pytest.mark.parametrize("psi", [0, 1, 10, 8_000_000_000, 7_000_000_000, 123_588_864])
+@pytest.mark.parametrize("N", [1, 3, 4, 8])
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+@pytest.mark.parametrize("gb,ob", [(2, 12), (4, 12), (2, 8)])
+def test_ledger_and_comm_match_oracle(zero_lib, oracle_mod, psi, N, stage, gb, ob):
+    assert zero_lib.zero_ledger(psi, N, stage, gb, ob) == oracle_mod.ledger_bytes(psi, N, stage,
+                                                                                   gb, ob)
+    assert zero_lib.zero_comm_volume(psi, N, stage) == oracle_mod.comm_volume(psi, N, stage)
+
+
+def test_ledger_printed_values(zero_lib):
+    assert [zero_lib.zero_ledger(8_000_000_000, 4, s) for s in range(4)] == \
+        [128_000_000_000, 56_000_000_000, 44_000_000_000, 32_000_000_000]
+    assert zero_lib.zero_ledger(-1, 4, 0) == -1 and zero_lib.zero_ledger(1, 4, 4) == -1
+
+
+def test_workspace_bytes(zero_lib):
+    Z = zero_lib
+    hp = Z.make_hparams()
+    base = Z.zero_workspace_bytes(1 << 20, hp, True)
+    assert base > 0 and base % 256 == 0
+    hp_skip = Z.make_hparams(skip_on_overflow=True)
+    # in place with skip needs the FP32 combined gradient; out of place does not
+    assert Z.zero_workspace_bytes(1 << 20, hp_skip, True) == base + 4 * (1 << 20)
+    assert Z.zero_workspace_bytes(1 << 20, hp_skip, False) == base
+    hp_clip = Z.make_hparams(max_grad_norm=1.0)
+    assert Z.zero_workspace_bytes(1 << 20, hp_clip, False) == base + 4 * (1 << 20)
+    assert Z.zero_workspace_bytes(-1, hp, True) == 0
+
+
+def test_status_strings(zero_lib):
+    Z = zero_lib
+    for code in (Z.ZERO_OK, Z.ZERO_STEP_SKIPPED, Z.ZERO_ERR_ARG, Z.ZERO_ERR_ALIGN, Z.ZERO_ERR_CUDA,
+                 Z.ZERO_ERR_TIMEOUT, Z.ZERO_ERR_WORKSPACE, Z.ZERO_ERR_OVERLAP):
+        assert Z.zero_status_str(code) != "unknown status"
+    assert Z.zero_status_str(12345) == "unknown status"
+
+
+# ---------------------------------------------------------------- argument checking
+# Fake device addresses: every call below must be rejected before any CUDA call.
+
+GB = 1 << 30
+
+
+def _call(Z, N=4, psi_pad=4 * 128 * 4, grads=None, master=1 * GB, m=2 * GB, v=3 * GB, w=4 * GB,
+          ws=5 * GB, ws_bytes=None, hp=None, loss_scale=1.0, dtype=None):
+    hp = hp or Z.make_hparams()
+    grads = grads if grads is not None else [6 * GB + i * GB // 4 for i in range(N)]
+    ws_bytes = Z.zero_workspace_bytes(psi_pad, hp, True) if ws_bytes is None else ws_bytes
+    return Z.zero_step(grads, Z.ZERO_GRAD_BF16 if dtype is None else dtype, master, m, v, w,
+                       psi_pad, N, hp, loss_scale, ws, ws_bytes, None, 0)
+
+
+def test_step_rejects_bad_sizes(zero_lib):
+    Z = zero_lib
+    assert _call(Z, N=0, grads=[]) == Z.ZERO_ERR_ARG
+    assert _call(Z, N=65, grads=[6 * GB] * 65) == Z.ZERO_ERR_ARG
+    assert _call(Z, psi_pad=4 * 128 * 4 + 8) == Z.ZERO_ERR_ARG      # not a multiple of N*128
+    assert _call(Z, psi_pad=-512) == Z.ZERO_ERR_ARG
+    assert _call(Z, dtype=7) == Z.ZERO_ERR_ARG
+    assert _call(Z, loss_scale=0.0) == Z.ZERO_ERR_ARG
+    assert _call(Z, loss_scale=float("inf")) == Z.ZERO_ERR_ARG
+
+
+@pytest.mark.parametrize("field,value", [("lr", -1.0), ("beta1", 1.0), ("beta2", -0.1),
+                                         ("eps", 0.0), ("weight_decay", float("nan")),
+                                         ("max_grad_norm", -1.0), ("step", 0),
+                                         ("skip_on_overflow", 2), ("reserved", 1),
+                                         ("bucket_elems", 12)])
+def test_step_rejects_bad_hparams(zero_lib, field, value):
+    Z = zero_lib
+    hp = Z.make_hparams()
+    setattr(hp, field, value)
+    assert _call(Z, hp=hp, ws_bytes=1 << 30) == Z.ZERO_ERR_ARG
+
+
+def test_step_rejects_null_and_misaligned(zero_lib):
+    Z = zero_lib
+    assert _call(Z, master=None) == Z.ZERO_ERR_ARG
+    assert _call(Z, grads=[6 * GB, None, 7 * GB, 8 * GB]) == Z.ZERO_ERR_ARG
+    assert _call(Z, m=2 * GB + 8) == Z.ZERO_ERR_ALIGN
+    assert _call(Z, grads=[6 * GB + 2, 7 * GB, 8 * GB, 9 * GB]) == Z.ZERO_ERR_ALIGN
+
+
+def test_step_rejects_bad_workspace(zero_lib):
+    Z = zero_lib
+    assert _call(Z, ws=None) == Z.ZERO_ERR_WORKSPACE
+    assert _call(Z, ws_bytes=100) == Z.ZERO_ERR_WORKSPACE
+    assert _call(Z, ws=5 * GB + 16) == Z.ZERO_ERR_WORKSPACE     # not 256-byte aligned
+    hp = Z.make_hparams(skip_on_overflow=True)                   # needs the FP32 copy in place
+    small = Z.zero_workspace_bytes(4 * 128 * 4, Z.make_hparams(), True)
+    assert _call(Z, hp=hp, ws_bytes=small) == Z.ZERO_ERR_WORKSPACE
+
+
+def test_step_rejects_overlap(zero_lib):
+    Z = zero_lib
+    assert _call(Z, m=1 * GB + 256) == Z.ZERO_ERR_OVERLAP          # m inside master
+    assert _call(Z, ws=4 * GB) == Z.ZERO_ERR_OVERLAP               # workspace on the weights
+    assert _call(Z, grads=[6 * GB, 6 * GB, 6 * GB, 3 * GB]) == Z.ZERO_ERR_OVERLAP  # grad on v
+    # read-only gradients may share memory: that passes validation and only then
+    # fails on this host without a GPU, or succeeds on a GPU -- so not tested here
+
+
+def test_step_into_rejects_aliasing(zero_lib):
+    Z = zero_lib
+    hp = Z.make_hparams(skip_on_overflow=True)
+    ws_bytes = Z.zero_workspace_bytes(512, hp, False)
+    g = [6 * GB]
+    rc = Z.zero_step_into(g, 0, 1 * GB, 2 * GB, 3 * GB, 4 * GB, 1 * GB, 8 * GB, 9 * GB, 10 * GB,
+                          128, 1, hp, 1.0, 11 * GB, ws_bytes, None, 0)
+    assert rc == Z.ZERO_ERR_OVERLAP
+    rc = Z.zero_step_into(g, 0, 1 * GB, 2 * GB, 3 * GB, 4 * GB, 7 * GB, 2 * GB + 64, 9 * GB,
+                          10 * GB, 128, 1, hp, 1.0, 11 * GB, ws_bytes, None, 0)
+    assert rc == Z.ZERO_ERR_OVERLAP
+    rc = Z.zero_step_into(g, 0, 1 * GB, 2 * GB, 3 * GB, None, 7 * GB, 8 * GB, 9 * GB,
+                          10 * GB, 128, 1, hp, 1.0, 11 * GB, ws_bytes, None, 0)
+    assert rc == Z.ZERO_ERR_ARG   # a skipped out-of-place step needs src_w
+
+
+def test_loss_scaler_matches_oracle_policy(oracle_mod):
+    from zero_sharded_mixed_04_gb300.optim import LossScaler
+    rng = np.random.default_rng(0)
+    flags = (rng.random(200) < 0.1).tolist()
+    ours = LossScaler(65536.0, True, interval=7)
+    scale, good = 65536.0, 0
+    for f in flags:
+        ours.update(f)
+        scale, good = oracle_mod.loss_scale_update(scale, good, f, 7, 0.5, 2.0)
+        assert (ours.scale, ours.good_steps) == (scale, good)
+    static = LossScaler(8.0, False)
+    static.update(True)
+    assert static.scale == 8.0
+
+
+def test_struct_layouts_match_the_header(zero_lib, tmp_path):
+    """The ctypes mirrors of the header's structs have the C sizes and offsets
+    (checked against a program gcc compiles from include/zero_gb300.h)."""
+    import subprocess
+    src = tmp_path / "layout.c"
+    structs = {"zero_layout": zero_lib.zero_layout, "zero_adam_hparams": zero_lib.zero_adam_hparams,
+               "zero_step_result": zero_lib.zero_step_result, "zero_plan": zero_lib.zero_plan}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "zero_gb300.h"',
+             "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["return 0; }"]
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", f"-I{os.path.join(ROOT, 'include')}", str(src), "-o",
+                    str(exe)], check=True)
+    out = dict(line.rsplit(" ", 1) for line in subprocess.run(
+        [str(exe)], check=True, capture_output=True, text=True).stdout.split("\n") if line)
+    for name, cls in structs.items():
+        assert int(out[name]) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(out[f"{name}.{field}"]) == getattr(cls, field).offset, f"{name}.{field}"
+
+
+def test_plan_rejects_misuse(zero_lib):
+    Z = zero_lib
+    hp = Z.make_hparams()
+    plan = Z.zero_plan()
+    n = 4 * 128 * 4
+    ws_bytes = Z.zero_workspace_bytes(n, hp, True)
+    rc = Z.zero_plan_init(plan, [6 * GB, 7 * GB, 8 * GB, 9 * GB], 0, 1 * GB, 2 * GB, 3 * GB, 4 * GB,
+                          1 * GB, 2 * GB, 3 * GB, 4 * GB, n, 4, hp, 1.0, 5 * GB, ws_bytes)
+    assert rc == Z.ZERO_OK and plan.state == 1 and plan.in_place == 1 and plan.two_pass == 0
+    # a bucket before begin, and an end before all buckets, are refused on the host
+    assert Z.zero_plan_bucket(plan, 0, n, None, 0) == Z.ZERO_ERR_ARG
+    assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG
+    bad = Z.zero_plan()
+    assert Z.zero_plan_begin(bad, 0) == Z.ZERO_ERR_ARG
+    # a plan for an out-of-place step with skip needs src_w
+    hp_skip = Z.make_hparams(skip_on_overflow=True)
+    rc = Z.zero_plan_init(plan, [6 * GB], 0, 1 * GB, 2 * GB, 3 * GB, None, 10 * GB, 11 * GB,
+                          12 * GB, 13 * GB, 128, 1, hp_skip, 1.0, 5 * GB,
+                          Z.zero_workspace_bytes(128, hp_skip, False))
+    assert rc == Z.ZERO_ERR_ARG

@@ -1,0 +1,256 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, on the same
+seeded inputs, element by element, over several steps.
+
+Sizes span several sweeps of the persistent grid plus ragged tails.  The
+matrix covers:
+  - N = 1..8 and a large N;
+  - BF16 and FP32 gradients;
+  - in place and out of place;
+  - the one-pass and two-pass forms, and buckets;
+  - weight decay, clipping, skip on overflow and the dynamic loss scale;
+  - non-finite gradients and the degenerate sizes (empty vector, one
+    parameter).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from parity_util import compare_result, compare_state, state_to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_state(master_np):
+    n = master_np.size
+    return {"master": master_np.copy(), "m": np.zeros(n, np.float32), "v": np.zeros(n, np.float32),
+            "w": np.zeros(n, np.uint16)}
+
+
+def _make_grads(N, psi, psi_pad, dtype, sigma, seed, gen_device="cpu"):
+    g = torch.Generator(device=gen_device)
+    g.manual_seed(seed)
+    out = []
+    for _ in range(N):
+        z = torch.zeros(psi_pad, dtype=torch.float32)
+        z[:psi] = torch.randn(psi, generator=g) * sigma
+        out.append(z.to(torch.bfloat16) if dtype == "bf16" else z)
+    return out
+
+
+def _np(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, wd=0.0,
+               clip=0.0, skip=False, out_of_place=False, bucket=0, loss_scale=1.0,
+               dynamic=False, growth_interval=2000, sigma=1e-3, bad_step=0, bad_value=np.inf,
+               seed=1234, api="step"):
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    unit = N * 128
+    psi_pad = -(-psi // unit) * unit
+    gm = torch.Generator()
+    gm.manual_seed(seed)
+    master = torch.zeros(psi_pad, dtype=torch.float32)
+    master[:psi] = torch.randn(psi, generator=gm) * 0.02
+    opt = ZeroAdam(psi_pad, N, dtype, lr=lr, weight_decay=wd, max_grad_norm=clip,
+                   skip_on_overflow=skip, bucket_elems=bucket, loss_scale=loss_scale,
+                   dynamic_loss_scale=dynamic, growth_interval=growth_interval,
+                   out_of_place=out_of_place, device=dev, master=master.to(dev))
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams(lr=lr, weight_decay=wd, max_grad_norm=clip)
+    o_t, o_scale, o_good = 0, loss_scale, 0
+    exact = clip == 0.0
+    for step in range(1, steps + 1):
+        grads = _make_grads(N, psi, psi_pad, dtype, sigma * o_scale, seed + step)
+        if step == bad_step and psi > 0:
+            grads[N - 1][min(psi - 1, 12345)] = float(bad_value)
+        res = opt.step([g.to(dev) for g in grads], api=api)
+        ores = oracle_mod.zero_step([_np(g) for g in grads], ref["master"], ref["m"], ref["v"],
+                                    ref["w"], hp, o_t + 1, o_scale, skip)
+        compare_result(res, ores)
+        if ores["applied"]:
+            o_t += 1
+        if dynamic:
+            o_scale, o_good = oracle_mod.loss_scale_update(o_scale, o_good,
+                                                           ores["found_nonfinite"],
+                                                           growth_interval, 0.5, 2.0)
+        assert opt.t == o_t and opt.scaler.scale == o_scale
+        compare_state(state_to_numpy(opt.state()), ref, exact, tag=f"step {step} ")
+    return opt, ref
+
+
+PSI_MULTI_SWEEP = 3_000_017   # several sweeps of the persistent grid, ragged tail
+PSI_SMALL = 200_003
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_one_pass_in_place(zero_lib, oracle_mod, N, dtype):
+    psi = PSI_MULTI_SWEEP if N in (4, 8) else PSI_SMALL
+    run_parity(zero_lib, oracle_mod, N=N, psi=psi, dtype=dtype)
+
+
+@pytest.mark.parametrize("N,dtype", [(4, "bf16"), (3, "fp32"), (8, "bf16")])
+def test_adamw_weight_decay(zero_lib, oracle_mod, N, dtype):
+    run_parity(zero_lib, oracle_mod, N=N, psi=PSI_SMALL, dtype=dtype, wd=0.1, steps=4)
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+@pytest.mark.parametrize("N,dtype", [(4, "bf16"), (8, "bf16"), (4, "fp32"), (5, "bf16")])
+def test_skip_on_overflow(zero_lib, oracle_mod, N, dtype, out_of_place):
+    """Step 2 gets one +inf; with the skip on it must leave the state
+    bit-unchanged and the next steps continue from there."""
+    run_parity(zero_lib, oracle_mod, N=N, psi=PSI_MULTI_SWEEP if N == 8 else PSI_SMALL,
+               dtype=dtype, steps=4, skip=True, out_of_place=out_of_place, bad_step=2,
+               loss_scale=1024.0, dynamic=True)
+
+
+@pytest.mark.parametrize("bad", [np.inf, -np.inf, np.nan])
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_nonfinite_values(zero_lib, oracle_mod, bad, out_of_place):
+    run_parity(zero_lib, oracle_mod, N=4, psi=PSI_SMALL, steps=3, skip=True,
+               out_of_place=out_of_place, bad_step=1, bad_value=bad)
+
+
+def test_nonfinite_without_skip_propagates(zero_lib, oracle_mod):
+    run_parity(zero_lib, oracle_mod, N=4, psi=PSI_SMALL, steps=2, skip=False, bad_step=1)
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+@pytest.mark.parametrize("N,dtype,clip", [(4, "fp32", 1.0), (4, "bf16", 0.01), (8, "bf16", 1e-4),
+                                          (3, "fp32", 1e9)])
+def test_global_norm_clip(zero_lib, oracle_mod, N, dtype, clip, out_of_place):
+    run_parity(zero_lib, oracle_mod, N=N, psi=PSI_MULTI_SWEEP if N == 8 else PSI_SMALL,
+               dtype=dtype, clip=clip, out_of_place=out_of_place, steps=3)
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_clip_with_skip(zero_lib, oracle_mod, out_of_place):
+    run_parity(zero_lib, oracle_mod, N=4, psi=PSI_SMALL, clip=0.5, skip=True,
+               out_of_place=out_of_place, bad_step=2, steps=3)
+
+
+@pytest.mark.parametrize("bucket", [8, 262_248, 1_000_000])
+@pytest.mark.parametrize("out_of_place,skip", [(False, False), (False, True), (True, True)])
+def test_buckets(zero_lib, oracle_mod, bucket, out_of_place, skip):
+    psi = PSI_SMALL if bucket == 8 else PSI_MULTI_SWEEP
+    run_parity(zero_lib, oracle_mod, N=8, psi=psi if bucket != 8 else 20_000, bucket=bucket,
+               out_of_place=out_of_place, skip=skip, steps=2, loss_scale=65536.0,
+               dynamic=True, bad_step=2 if skip else 0)
+
+
+def test_dynamic_loss_scale_growth(zero_lib, oracle_mod):
+    run_parity(zero_lib, oracle_mod, N=2, psi=20_000, steps=7, skip=True, out_of_place=True,
+               loss_scale=256.0, dynamic=True, growth_interval=2, bad_step=4)
+
+
+@pytest.mark.parametrize("psi", [1, 127, 128, 129, 1023])
+def test_tiny_and_ragged(zero_lib, oracle_mod, psi):
+    run_parity(zero_lib, oracle_mod, N=4, psi=psi, steps=2)
+    run_parity(zero_lib, oracle_mod, N=3, psi=psi, steps=2, dtype="fp32", clip=1e-3)
+
+
+def test_many_ranks(zero_lib, oracle_mod):
+    run_parity(zero_lib, oracle_mod, N=64, psi=100_000, steps=2)
+    run_parity(zero_lib, oracle_mod, N=13, psi=100_000, steps=2, dtype="fp32", skip=True,
+               bad_step=2)
+
+
+def test_empty_vector(zero_lib):
+    Z = zero_lib
+    hp = Z.make_hparams(skip_on_overflow=True)
+    ws = torch.empty(Z.zero_workspace_bytes(0, hp, True), dtype=torch.uint8, device="cuda")
+    rc = Z.zero_step([None, None], Z.ZERO_GRAD_BF16, None, None, None, None, 0, 2, hp, 1.0, ws,
+                     ws.numel(), None, None)
+    assert rc == Z.ZERO_OK
+
+
+def test_blocking_call_returns_status(zero_lib):
+    """With no result pointer the call waits and returns the step status."""
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, n = 2, 2 * 128 * 4
+    grads = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for _ in range(N)]
+    grads[1][5] = float("nan")
+    st = [torch.zeros(n, dtype=torch.float32, device=dev) for _ in range(3)]
+    w = torch.zeros(n, dtype=torch.int16, device=dev)
+    hp = Z.make_hparams(skip_on_overflow=True)
+    ws = torch.empty(Z.zero_workspace_bytes(n, hp, True), dtype=torch.uint8, device=dev)
+    rc = Z.zero_step(grads, Z.ZERO_GRAD_BF16, *st, w, n, N, hp, 1.0, ws, ws.numel(), None, None)
+    assert rc == Z.ZERO_STEP_SKIPPED
+    grads[1][5] = 0.0
+    rc = Z.zero_step(grads, Z.ZERO_GRAD_BF16, *st, w, n, N, hp, 1.0, ws, ws.numel(), None, None)
+    assert rc == Z.ZERO_OK
+
+
+def test_launch_count_grows(zero_lib):
+    Z = zero_lib
+    before = Z.zero_launch_count()
+    test_blocking_call_returns_status(zero_lib)
+    assert Z.zero_launch_count() >= before + 4
+
+
+@pytest.mark.parametrize("out_of_place,skip,clip", [(False, False, 0.0), (True, True, 0.0),
+                                                   (False, True, 0.0), (True, False, 0.3)])
+def test_plan_api(zero_lib, oracle_mod, out_of_place, skip, clip):
+    """The bucketed entry points give the same result as zero_step."""
+    run_parity(zero_lib, oracle_mod, N=8, psi=PSI_MULTI_SWEEP, bucket=400_000,
+               out_of_place=out_of_place, skip=skip, clip=clip, steps=3, api="plan",
+               bad_step=2 if skip else 0, loss_scale=4096.0, dynamic=skip)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_plan_two_staging_slots(zero_lib, oracle_mod, dtype):
+    """Gradients streamed bucket by bucket through two device slots (one in
+    use while the other loads) give the state the whole-vector step gives."""
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, psi, bucket = 4, 1_000_003, 131_072
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    grads = _make_grads(N, psi, psi_pad, dtype, 1e-3, 99)
+    host = [g.pin_memory() for g in grads]
+    master = torch.randn(psi_pad, generator=torch.Generator().manual_seed(5)) * 0.02
+    master[psi:] = 0
+    st = {k: torch.zeros(psi_pad, dtype=torch.float32, device=dev) for k in ("m", "v")}
+    st["master"] = master.to(dev)
+    w = torch.zeros(psi_pad, dtype=torch.int16, device=dev)
+    hp = Z.make_hparams(skip_on_overflow=False)
+    ws = torch.empty(Z.zero_workspace_bytes(psi_pad, hp, True), dtype=torch.uint8, device=dev)
+    slots = [[torch.empty(bucket, dtype=tdt, device=dev) for _ in range(N)] for _ in range(2)]
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    freed = [torch.cuda.Event(), torch.cuda.Event()]
+    loaded = [torch.cuda.Event(), torch.cuda.Event()]
+    plan = Z.zero_plan()
+    assert Z.zero_plan_init(plan, [None] * N, Z.ZERO_GRAD_BF16 if dtype == "bf16" else
+                            Z.ZERO_GRAD_FP32, st["master"], st["m"], st["v"], w, st["master"],
+                            st["m"], st["v"], w, psi_pad, N, hp, 1.0, ws, ws.numel()) == 0
+    assert Z.zero_plan_begin(plan, compute) == 0
+    for k, b0 in enumerate(range(0, psi_pad, bucket)):
+        b1 = min(psi_pad, b0 + bucket)
+        slot = k % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(freed[slot])
+            for i in range(N):
+                slots[slot][i][:b1 - b0].copy_(host[i][b0:b1], non_blocking=True)
+            loaded[slot].record(copy)
+        compute.wait_event(loaded[slot])
+        assert Z.zero_plan_bucket(plan, b0, b1, [t for t in slots[slot]], compute) == 0
+        freed[slot].record(compute)
+    res = Z.zero_step_result()
+    res_t = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+    assert Z.zero_plan_end(plan, res_t, compute) == 0
+    torch.cuda.synchronize()
+    ref = _oracle_state(master.numpy())
+    ores = oracle_mod.zero_step([_np(g) for g in grads], ref["master"], ref["m"], ref["v"],
+                                ref["w"], oracle_mod.Hparams(), 1, 1.0, False)
+    assert int(res_t[0]) == 0 and ores["applied"]
+    got = {"master": st["master"].cpu().numpy(), "m": st["m"].cpu().numpy(),
+           "v": st["v"].cpu().numpy(), "w": w.cpu().numpy().view(np.uint16)}
+    compare_state(got, ref, exact=True)

@@ -1,0 +1,781 @@
+// zero_step.cu -- the ZeRO update step on one GB300 (sm_103a).
+//
+// One step = reduce-scatter of N ranks' gradients with batch-mean scaling,
+// owner-local mixed-precision Adam on the FP32 master/m/v slice, BF16 cast and
+// all-gather into the full working-weight view.  Sources:
+//   - lecture deck "RC-T2", note N48.  The reduction adds contributions of the
+//     same parameter only, scaled to match a batch-mean loss.  The owner
+//     updates its slice with its own master weight and m/v.  The next
+//     all-gather fetches the updated version.
+//   - topic page "Putting the training ledger onto multiple devices", section
+//     "one full ZeRO-3 computation": reduce-scatter/all-gather as data
+//     semantics.
+//   - blog post "Data parallelism and ZeRO: how much each of the three stages
+//     saves", section "three stages": ZeRO-1/2 reduce-scatter the gradient,
+//     step 1/N of the FP32 state, all-gather the BF16 weights.
+//
+// The N simulated ranks share this device's memory, so a collective is a
+// memory access pattern.  For every element j of owner r's slice, the owner
+// reads grads[0..N-1][j] (the reduce-scatter).  It writes w[j] into the one
+// full-view buffer (the all-gather).  All owners run concurrently: the grid
+// walks the whole flat vector, and each 8-element group belongs to exactly
+// one owner, because every slice is a multiple of 128 elements.
+//
+// The path is bound by HBM bandwidth (about 0.5 flop per byte), so nothing
+// here uses tensor cores.  Each thread moves 16-byte vectors.  Every load of
+// a group is issued before its arithmetic.  The arithmetic uses the explicit
+// round-to-nearest intrinsics, so no multiply-add is ever contracted: each
+// element is rounded operator by operator.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "zero_gb300.h"
+
+namespace {
+
+constexpr int kThreads = 256;             // threads per CTA of the streaming kernels
+constexpr int kVec = 8;                   // elements per thread per group (16 B of BF16)
+constexpr int kMaxGrid = 2048;            // CTAs per launch, at most
+constexpr int kFinalizeThreads = 1024;
+constexpr size_t kCtrlBytes = 256;
+constexpr size_t kPartialsOffset = kCtrlBytes;
+constexpr size_t kGradOffset = kPartialsOffset + kMaxGrid * sizeof(double);  // 256-B aligned
+
+std::atomic<uint64_t> g_launches{0};
+
+// Control block at the start of the workspace.  It is zeroed at the start of
+// every step.
+struct Ctrl {
+    unsigned int nonfinite;    // OR over all elements of "combined gradient is inf/NaN"
+    int skip;                  // decided by the finalize kernel
+    float clip_coef;           // decided by the finalize kernel
+    float grad_norm;
+    zero_step_result result;   // the outcome, when the caller passes no result pointer
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+static_assert(kGradOffset % 256 == 0, "gradient workspace alignment");
+
+// Per-step FP32 scalars, each rounded once from FP64.
+struct Scalars {
+    float inv;        // 1 / (N * loss_scale)
+    float b1, omb1;   // beta1, 1 - beta1
+    float b2, omb2;   // beta2, 1 - beta2
+    float eps;
+    float step_size;  // lr / (1 - beta1^t)
+    float sbc2;       // sqrt(1 - beta2^t)
+    float decay;      // 1 - lr * weight_decay
+    int use_decay;
+};
+
+struct StepArgs {
+    const void* grads[ZERO_MAX_RANKS];
+    const float* src_master;
+    const float* src_m;
+    const float* src_v;
+    const uint16_t* src_w;
+    float* dst_master;
+    float* dst_m;
+    float* dst_v;
+    uint16_t* dst_w;
+    float* gws;          // FP32 combined gradient (two-pass form)
+    double* partials;    // one FP64 sum of squares per CTA
+    Ctrl* ctrl;
+    Scalars s;
+    int64_t begin;       // first element of this launch (a multiple of kVec)
+    int64_t n8;          // groups of kVec elements in this launch
+    int64_t gbase;       // flat index of grads[i][0] (the bucket start for a staging slot)
+    int32_t N;
+    int32_t clip;        // 1: multiply the gradient by ctrl->clip_coef before Adam
+};
+
+// ------------------------------------------------------------------ element math
+
+__device__ __forceinline__ bool is_nonfinite(float x) {
+    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
+}
+
+// BF16 is the top half of an FP32 word; element 2q of a 16-byte vector is the
+// low half of 32-bit word q.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest, ties to even
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Owner update of one element: AdamW with bias correction, every operator
+// rounded to FP32 on its own.
+__device__ __forceinline__ void adam_element(float g, float& p, float& m, float& v,
+                                             const Scalars& s) {
+    if (s.use_decay) p = __fmul_rn(p, s.decay);
+    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sbc2), s.eps);
+    p = __fsub_rn(p, __fmul_rn(s.step_size, __fdiv_rn(m, den)));
+}
+
+// ------------------------------------------------------------------ vector loads
+
+template <bool kBF16>
+struct GradVec;
+
+template <>
+struct GradVec<true> {
+    uint4 r;
+    __device__ __forceinline__ void load(const void* base, int64_t j) {
+        r = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + j));
+    }
+    __device__ __forceinline__ void add_to(float (&g)[kVec]) const {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            g[2 * q] = __fadd_rn(g[2 * q], bf16_lo(w[q]));
+            g[2 * q + 1] = __fadd_rn(g[2 * q + 1], bf16_hi(w[q]));
+        }
+    }
+};
+
+template <>
+struct GradVec<false> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const void* base, int64_t j) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + j);
+        a = __ldcs(p);
+        b = __ldcs(p + 1);
+    }
+    __device__ __forceinline__ void add_to(float (&g)[kVec]) const {
+        g[0] = __fadd_rn(g[0], a.x); g[1] = __fadd_rn(g[1], a.y);
+        g[2] = __fadd_rn(g[2], a.z); g[3] = __fadd_rn(g[3], a.w);
+        g[4] = __fadd_rn(g[4], b.x); g[5] = __fadd_rn(g[5], b.y);
+        g[6] = __fadd_rn(g[6], b.z); g[7] = __fadd_rn(g[7], b.w);
+    }
+};
+
+// The reduce-scatter of one 8-element group: every rank's contribution to
+// these same elements, added in rank order starting from +0.  NT > 0 fixes N
+// at compile time (all N loads in flight together); NT == 0 takes a.N.
+template <int NT, bool kBF16>
+__device__ __forceinline__ void combine(const StepArgs& a, int64_t j, float (&g)[kVec]) {
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) g[e] = 0.0f;
+    if constexpr (NT > 0) {
+        GradVec<kBF16> raw[NT];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) raw[i].load(a.grads[i], j - a.gbase);
+#pragma unroll
+        for (int i = 0; i < NT; ++i) raw[i].add_to(g);
+    } else {
+        int i = 0;
+        for (; i + 4 <= a.N; i += 4) {
+            GradVec<kBF16> raw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) raw[k].load(a.grads[i + k], j - a.gbase);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) raw[k].add_to(g);
+        }
+        for (; i < a.N; ++i) {
+            GradVec<kBF16> raw;
+            raw.load(a.grads[i], j - a.gbase);
+            raw.add_to(g);
+        }
+    }
+}
+
+__device__ __forceinline__ void load8(const float* base, int64_t j, float (&x)[kVec]) {
+    const float4* p = reinterpret_cast<const float4*>(base + j);
+    const float4 u = __ldcs(p), w = __ldcs(p + 1);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
+}
+
+__device__ __forceinline__ void store8(float* base, int64_t j, const float (&x)[kVec]) {
+    float4* p = reinterpret_cast<float4*>(base + j);
+    __stcs(p, make_float4(x[0], x[1], x[2], x[3]));
+    __stcs(p + 1, make_float4(x[4], x[5], x[6], x[7]));
+}
+
+__device__ __forceinline__ void store_w8(uint16_t* base, int64_t j, const float (&p)[kVec]) {
+    const uint4 packed = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                                    pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+    __stcs(reinterpret_cast<uint4*>(base + j), packed);
+}
+
+// End of a CTA's share: publish the overflow flag (one atomic per warp that
+// saw a non-finite value) and add the CTA's sum of squares to its FP64 slot.
+// Warp-shuffle tree, then the warps in order, so the sum is deterministic.
+__device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, double sumsq) {
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->nonfinite, 1u);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, off);
+    __shared__ double warp_sum[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = sumsq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) t += warp_sum[w];
+        a.partials[blockIdx.x] += t;  // launches of one step are ordered on one stream
+    }
+}
+
+// ------------------------------------------------------------------ kernels
+
+// One pass: reduce-scatter + scale + check + Adam + BF16 all-gather.  Reads
+// src_*, writes dst_* (the same arrays for an in-place step).
+template <int NT, bool kBF16>
+__global__ void __launch_bounds__(kThreads) zero_fused_kernel(const __grid_constant__ StepArgs a) {
+    unsigned bad = 0;
+    double sumsq = 0.0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+         q += stride) {
+        const int64_t j = a.begin + q * kVec;
+        float p[kVec], m[kVec], v[kVec], g[kVec];
+        load8(a.src_master, j, p);
+        load8(a.src_m, j, m);
+        load8(a.src_v, j, v);
+        combine<NT, kBF16>(a, j, g);
+        float sq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            const float gs = __fmul_rn(g[e], a.s.inv);
+            bad |= is_nonfinite(gs) ? 1u : 0u;
+            sq = fmaf(gs, gs, sq);
+            adam_element(gs, p[e], m[e], v[e], a.s);
+        }
+        sumsq += static_cast<double>(sq);
+        store8(a.dst_master, j, p);
+        store8(a.dst_m, j, m);
+        store8(a.dst_v, j, v);
+        store_w8(a.dst_w, j, p);
+    }
+    finish_cta(a, bad, sumsq);
+}
+
+// First pass of the two-pass form: reduce-scatter + scale + check, writing the
+// FP32 combined gradient to the workspace.
+template <int NT, bool kBF16>
+__global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_constant__ StepArgs a) {
+    unsigned bad = 0;
+    double sumsq = 0.0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+         q += stride) {
+        const int64_t j = a.begin + q * kVec;
+        float g[kVec];
+        combine<NT, kBF16>(a, j, g);
+        float sq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            g[e] = __fmul_rn(g[e], a.s.inv);
+            bad |= is_nonfinite(g[e]) ? 1u : 0u;
+            sq = fmaf(g[e], g[e], sq);
+        }
+        sumsq += static_cast<double>(sq);
+        store8(a.gws, j, g);
+    }
+    finish_cta(a, bad, sumsq);
+}
+
+__device__ __forceinline__ void copy_state(const StepArgs& a) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+         q += stride) {
+        const int64_t j = a.begin + q * kVec;
+        float x[kVec];
+        load8(a.src_master, j, x);
+        store8(a.dst_master, j, x);
+        load8(a.src_m, j, x);
+        store8(a.dst_m, j, x);
+        load8(a.src_v, j, x);
+        store8(a.dst_v, j, x);
+        __stcs(reinterpret_cast<uint4*>(a.dst_w + j),
+               __ldcs(reinterpret_cast<const uint4*>(a.src_w + j)));
+    }
+}
+
+// Second pass of the two-pass form: Adam + BF16 all-gather from the
+// workspace's combined gradient, unless the step was skipped.  A skipped
+// out-of-place step copies src to dst instead.
+__global__ void __launch_bounds__(kThreads) zero_update_kernel(const __grid_constant__ StepArgs a) {
+    if (a.ctrl->skip) {
+        if (a.dst_master != a.src_master) copy_state(a);
+        return;
+    }
+    const float coef = a.ctrl->clip_coef;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+         q += stride) {
+        const int64_t j = a.begin + q * kVec;
+        float p[kVec], m[kVec], v[kVec], g[kVec];
+        load8(a.src_master, j, p);
+        load8(a.src_m, j, m);
+        load8(a.src_v, j, v);
+        load8(a.gws, j, g);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            const float gs = a.clip ? __fmul_rn(g[e], coef) : g[e];
+            adam_element(gs, p[e], m[e], v[e], a.s);
+        }
+        store8(a.dst_master, j, p);
+        store8(a.dst_m, j, m);
+        store8(a.dst_v, j, v);
+        store_w8(a.dst_w, j, p);
+    }
+}
+
+// After a one-pass out-of-place step: a skipped step must leave dst equal to
+// src, so copy it; an applied step needs nothing.
+__global__ void __launch_bounds__(kThreads) zero_restore_kernel(const __grid_constant__ StepArgs a) {
+    if (a.ctrl->skip) copy_state(a);
+}
+
+// Step-wide decision: sums the per-CTA partials in a fixed order, forms the
+// norm and clip coefficient, decides the skip, and writes the result.
+__global__ void __launch_bounds__(kFinalizeThreads)
+zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int skip_on_overflow,
+                     zero_step_result* result) {
+    __shared__ double s[kFinalizeThreads];
+    double t = 0.0;
+    for (int i = threadIdx.x; i < kMaxGrid; i += kFinalizeThreads) t += partials[i];
+    s[threadIdx.x] = t;
+    __syncthreads();
+    for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) s[threadIdx.x] += s[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double sumsq = s[0];
+        const double norm = sqrt(sumsq);
+        const int nonfinite = ctrl->nonfinite != 0u;
+        const int skip = (skip_on_overflow && nonfinite) ? 1 : 0;
+        float coef = 1.0f;
+        if (max_norm > 0.0 && !skip) {
+            const double c = max_norm / (norm + 1e-6);
+            coef = (c < 1.0) ? static_cast<float>(c) : 1.0f;  // a NaN norm compares false
+        }
+        ctrl->skip = skip;
+        ctrl->clip_coef = coef;
+        ctrl->grad_norm = static_cast<float>(norm);
+        zero_step_result r;
+        r.status = skip ? ZERO_STEP_SKIPPED : ZERO_OK;
+        r.found_nonfinite = static_cast<uint32_t>(nonfinite);
+        r.grad_norm = static_cast<float>(norm);
+        r.clip_coef = coef;
+        *result = r;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+using StepKernel = void (*)(StepArgs);
+
+template <int NT, bool B>
+struct FusedK {
+    static constexpr StepKernel fn = zero_fused_kernel<NT, B>;
+};
+template <int NT, bool B>
+struct ReduceK {
+    static constexpr StepKernel fn = zero_reduce_kernel<NT, B>;
+};
+
+template <template <int, bool> class K>
+StepKernel pick(int N, bool bf16) {
+    switch (N) {
+        case 1: return bf16 ? K<1, true>::fn : K<1, false>::fn;
+        case 2: return bf16 ? K<2, true>::fn : K<2, false>::fn;
+        case 4: return bf16 ? K<4, true>::fn : K<4, false>::fn;
+        case 8: return bf16 ? K<8, true>::fn : K<8, false>::fn;
+        default: return bf16 ? K<0, true>::fn : K<0, false>::fn;
+    }
+}
+
+// CTAs per SM for a kernel on a device, measured once and cached.
+int resident_ctas(const void* fn, int device, int threads) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair(fn, device);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1)
+        n = 1;
+    cache[key] = n;
+    return n;
+}
+
+int sm_count(int device) {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(device);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
+        n = 1;
+    cache[device] = n;
+    return n;
+}
+
+// Persistent grid: as many CTAs as fit on the device at once (a multiple of
+// the SM count), fewer if the range is small.
+int grid_for(const void* fn, int device, int64_t n8) {
+    const int64_t full = static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, kThreads);
+    const int64_t need = (n8 + kThreads - 1) / kThreads;
+    int64_t g = need < full ? need : full;
+    if (g > kMaxGrid) g = kMaxGrid;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+
+bool launch(StepKernel fn, int device, const StepArgs& a, cudaStream_t stream) {
+    const int grid = grid_for(reinterpret_cast<const void*>(fn), device, a.n8);
+    fn<<<grid, kThreads, 0, stream>>>(a);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Span {
+    uintptr_t lo, hi;
+    bool written;
+};
+
+bool overlaps(const Span& x, const Span& y) { return x.lo < y.hi && y.lo < x.hi; }
+
+bool disjoint(const Span* s, int n) {
+    for (int i = 0; i < n; ++i)
+        for (int k = i + 1; k < n; ++k) {
+            if (!s[i].written && !s[k].written) continue;  // read-only buffers may share memory
+            if (overlaps(s[i], s[k])) return false;
+        }
+    return true;
+}
+
+bool valid_hparams(const zero_adam_hparams* hp) {
+    if (hp == nullptr) return false;
+    auto finite = [](double x) { return std::isfinite(x); };
+    return finite(hp->lr) && hp->lr >= 0.0 && finite(hp->beta1) && hp->beta1 >= 0.0 &&
+           hp->beta1 < 1.0 && finite(hp->beta2) && hp->beta2 >= 0.0 && hp->beta2 < 1.0 &&
+           finite(hp->eps) && hp->eps > 0.0 && finite(hp->weight_decay) &&
+           hp->weight_decay >= 0.0 && finite(hp->max_grad_norm) && hp->max_grad_norm >= 0.0 &&
+           hp->step >= 1 && (hp->skip_on_overflow == 0 || hp->skip_on_overflow == 1) &&
+           hp->reserved == 0 && hp->bucket_elems >= 0 && hp->bucket_elems % ZERO_BUCKET_ALIGN == 0;
+}
+
+bool needs_two_passes(const zero_adam_hparams* hp, bool in_place) {
+    return hp->max_grad_norm > 0.0 || (in_place && hp->skip_on_overflow);
+}
+
+Scalars make_scalars(const zero_adam_hparams* hp, int32_t N, float loss_scale) {
+    Scalars s;
+    const double t = static_cast<double>(hp->step);
+    s.inv = static_cast<float>(1.0 / (static_cast<double>(N) * static_cast<double>(loss_scale)));
+    s.b1 = static_cast<float>(hp->beta1);
+    s.omb1 = static_cast<float>(1.0 - hp->beta1);
+    s.b2 = static_cast<float>(hp->beta2);
+    s.omb2 = static_cast<float>(1.0 - hp->beta2);
+    s.eps = static_cast<float>(hp->eps);
+    s.step_size = static_cast<float>(hp->lr / (1.0 - std::pow(hp->beta1, t)));
+    s.sbc2 = static_cast<float>(std::sqrt(1.0 - std::pow(hp->beta2, t)));
+    s.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
+    s.use_decay = hp->weight_decay != 0.0 ? 1 : 0;
+    return s;
+}
+
+size_t workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, bool in_place) {
+    size_t b = kGradOffset;
+    if (needs_two_passes(hp, in_place)) b += static_cast<size_t>(psi_pad) * sizeof(float);
+    return b;
+}
+
+size_t grad_elem_bytes(int32_t dtype) { return dtype == ZERO_GRAD_BF16 ? 2u : 4u; }
+
+// The buffers a step writes, as spans (for the overlap checks).
+int written_spans(const zero_plan* p, Span* out) {
+    const uintptr_t n = static_cast<uintptr_t>(p->psi_pad);
+    int k = 0;
+    auto add = [&](const void* ptr, uintptr_t bytes) {
+        if (ptr != nullptr)
+            out[k++] = Span{reinterpret_cast<uintptr_t>(ptr), reinterpret_cast<uintptr_t>(ptr) + bytes,
+                            true};
+    };
+    add(p->dst_master, 4 * n);
+    add(p->dst_m, 4 * n);
+    add(p->dst_v, 4 * n);
+    add(p->dst_w_bf16, 2 * n);
+    add(p->workspace, workspace_bytes(p->psi_pad, &p->hp, p->in_place != 0));
+    return k;
+}
+
+StepArgs base_args(const zero_plan* p) {
+    char* ws = static_cast<char*>(p->workspace);
+    StepArgs a{};
+    for (int i = 0; i < p->N; ++i) a.grads[i] = p->grads[i];
+    a.src_master = p->src_master;
+    a.src_m = p->src_m;
+    a.src_v = p->src_v;
+    a.src_w = p->src_w_bf16;
+    a.dst_master = p->dst_master;
+    a.dst_m = p->dst_m;
+    a.dst_v = p->dst_v;
+    a.dst_w = p->dst_w_bf16;
+    a.gws = reinterpret_cast<float*>(ws + kGradOffset);
+    a.partials = reinterpret_cast<double*>(ws + kPartialsOffset);
+    a.ctrl = reinterpret_cast<Ctrl*>(ws);
+    a.s = make_scalars(&p->hp, p->N, p->loss_scale);
+    a.N = p->N;
+    a.clip = p->hp.max_grad_norm > 0.0 ? 1 : 0;
+    a.gbase = 0;
+    return a;
+}
+
+int plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
+              const float* src_master, const float* src_m, const float* src_v,
+              const uint16_t* src_w, float* dst_master, float* dst_m, float* dst_v,
+              uint16_t* dst_w, int64_t psi_pad, int32_t N, const zero_adam_hparams* hp,
+              float loss_scale, void* workspace, size_t workspace_bytes_given,
+              bool allow_null_grads) {
+    if (plan == nullptr) return ZERO_ERR_ARG;
+    const bool in_place = (dst_master == src_master);
+    if (grads == nullptr || N < 1 || N > ZERO_MAX_RANKS || psi_pad < 0 ||
+        (grad_dtype != ZERO_GRAD_BF16 && grad_dtype != ZERO_GRAD_FP32) || !valid_hparams(hp) ||
+        !(loss_scale > 0.0f) || !std::isfinite(loss_scale))
+        return ZERO_ERR_ARG;
+    if (psi_pad % (static_cast<int64_t>(N) * ZERO_PAD_UNIT) != 0) return ZERO_ERR_ARG;
+    const bool have_data = psi_pad > 0;
+    const void* bufs[] = {src_master, src_m, src_v, dst_master, dst_m, dst_v, dst_w};
+    for (const void* p : bufs)
+        if (have_data && p == nullptr) return ZERO_ERR_ARG;
+    if (!in_place && hp->skip_on_overflow && have_data && src_w == nullptr) return ZERO_ERR_ARG;
+    if (in_place && (src_m != dst_m || src_v != dst_v)) return ZERO_ERR_ARG;
+    for (int i = 0; i < N; ++i) {
+        if (have_data && grads[i] == nullptr && !allow_null_grads) return ZERO_ERR_ARG;
+        if (!aligned(grads[i], ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+    }
+    for (const void* p : bufs)
+        if (!aligned(p, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+    if (!aligned(src_w, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+    const size_t need = workspace_bytes(psi_pad, hp, in_place);
+    if (workspace == nullptr || workspace_bytes_given < need || !aligned(workspace, 256))
+        return ZERO_ERR_WORKSPACE;
+
+    zero_plan p{};
+    for (int i = 0; i < N; ++i) p.grads[i] = grads[i];
+    p.src_master = src_master;
+    p.src_m = src_m;
+    p.src_v = src_v;
+    p.src_w_bf16 = src_w;
+    p.dst_master = dst_master;
+    p.dst_m = dst_m;
+    p.dst_v = dst_v;
+    p.dst_w_bf16 = dst_w;
+    p.workspace = workspace;
+    p.workspace_bytes = workspace_bytes_given;
+    p.psi_pad = psi_pad;
+    p.cursor = 0;
+    p.hp = *hp;
+    p.loss_scale = loss_scale;
+    p.grad_dtype = grad_dtype;
+    p.N = N;
+    p.in_place = in_place ? 1 : 0;
+    p.two_pass = needs_two_passes(hp, in_place) ? 1 : 0;
+    p.state = 1;
+
+    if (have_data) {
+        const uintptr_t n = static_cast<uintptr_t>(psi_pad);
+        Span sp[ZERO_MAX_RANKS + 9];
+        int k = written_spans(&p, sp);
+        auto add = [&](const void* ptr, uintptr_t bytes) {
+            if (ptr != nullptr)
+                sp[k++] = Span{reinterpret_cast<uintptr_t>(ptr),
+                               reinterpret_cast<uintptr_t>(ptr) + bytes, false};
+        };
+        for (int i = 0; i < N; ++i) add(grads[i], n * grad_elem_bytes(grad_dtype));
+        if (!in_place) {
+            add(src_master, 4 * n);
+            add(src_m, 4 * n);
+            add(src_v, 4 * n);
+            if (hp->skip_on_overflow) add(src_w, 2 * n);
+        }
+        if (!disjoint(sp, k)) return ZERO_ERR_OVERLAP;
+    }
+    *plan = p;
+    return ZERO_OK;
+}
+
+int plan_begin(zero_plan* p, void* stream) {
+    if (p == nullptr || p->state < 1) return ZERO_ERR_ARG;
+    if (cudaMemsetAsync(p->workspace, 0, kGradOffset, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return ZERO_ERR_CUDA;
+    p->cursor = 0;
+    p->state = 2;
+    return ZERO_OK;
+}
+
+int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* bucket_grads,
+                void* stream) {
+    if (p == nullptr || p->state != 2) return ZERO_ERR_ARG;
+    if (begin != p->cursor || end <= begin || end > p->psi_pad ||
+        (end % ZERO_BUCKET_ALIGN != 0 && end != p->psi_pad))
+        return ZERO_ERR_ARG;
+    StepArgs a = base_args(p);
+    if (bucket_grads != nullptr) {
+        Span written[5];
+        const int nw = written_spans(p, written);
+        const uintptr_t bytes = static_cast<uintptr_t>(end - begin) * grad_elem_bytes(p->grad_dtype);
+        for (int i = 0; i < p->N; ++i) {
+            if (bucket_grads[i] == nullptr) return ZERO_ERR_ARG;
+            if (!aligned(bucket_grads[i], ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+            const Span g{reinterpret_cast<uintptr_t>(bucket_grads[i]),
+                         reinterpret_cast<uintptr_t>(bucket_grads[i]) + bytes, false};
+            for (int k = 0; k < nw; ++k)
+                if (overlaps(g, written[k])) return ZERO_ERR_OVERLAP;
+            a.grads[i] = bucket_grads[i];
+        }
+        a.gbase = begin;
+    } else {
+        for (int i = 0; i < p->N; ++i)
+            if (p->grads[i] == nullptr) return ZERO_ERR_ARG;
+    }
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
+    a.begin = begin;
+    a.n8 = (end - begin) / kVec;
+    const bool bf16 = p->grad_dtype == ZERO_GRAD_BF16;
+    const StepKernel fn = p->two_pass ? pick<ReduceK>(p->N, bf16) : pick<FusedK>(p->N, bf16);
+    if (!launch(fn, device, a, static_cast<cudaStream_t>(stream))) return ZERO_ERR_CUDA;
+    p->cursor = end;
+    return ZERO_OK;
+}
+
+int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
+    if (p == nullptr || p->state != 2 || p->cursor != p->psi_pad) return ZERO_ERR_ARG;
+    zero_step_result* result_dev = nullptr;
+    if (result != nullptr) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, result) != cudaSuccess || attr.devicePointer == nullptr) {
+            cudaGetLastError();  // clear the error that query may leave behind
+            return ZERO_ERR_ARG;
+        }
+        result_dev = static_cast<zero_step_result*>(attr.devicePointer);
+    }
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_handle);
+    StepArgs a = base_args(p);
+    Ctrl* ctrl = a.ctrl;
+    if (result_dev == nullptr) result_dev = &ctrl->result;
+
+    zero_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(
+        ctrl, a.partials, p->hp.max_grad_norm, p->hp.skip_on_overflow, result_dev);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
+
+    a.begin = 0;
+    a.n8 = p->psi_pad / kVec;
+    if (p->two_pass) {
+        if (!launch(zero_update_kernel, device, a, stream)) return ZERO_ERR_CUDA;
+    } else if (!p->in_place && p->hp.skip_on_overflow) {
+        if (!launch(zero_restore_kernel, device, a, stream)) return ZERO_ERR_CUDA;
+    }
+    p->state = 1;
+
+    if (result == nullptr) {
+        zero_step_result host;
+        if (cudaMemcpyAsync(&host, &ctrl->result, sizeof host, cudaMemcpyDeviceToHost, stream) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return ZERO_ERR_CUDA;
+        return host.status;
+    }
+    return ZERO_OK;
+}
+
+// zero_step and zero_step_into: one plan, walked bucket by bucket.
+int run_step(const void* const* grads, int32_t grad_dtype, const float* src_master,
+             const float* src_m, const float* src_v, const uint16_t* src_w, float* dst_master,
+             float* dst_m, float* dst_v, uint16_t* dst_w, int64_t psi_pad, int32_t N,
+             const zero_adam_hparams* hp, float loss_scale, void* workspace,
+             size_t workspace_bytes_given, zero_step_result* result, void* stream) {
+    zero_plan plan;
+    int rc = plan_init(&plan, grads, grad_dtype, src_master, src_m, src_v, src_w, dst_master, dst_m,
+                       dst_v, dst_w, psi_pad, N, hp, loss_scale, workspace, workspace_bytes_given,
+                       false);
+    if (rc != ZERO_OK) return rc;
+    if ((rc = plan_begin(&plan, stream)) != ZERO_OK) return rc;
+    const int64_t bucket = hp->bucket_elems > 0 ? hp->bucket_elems : psi_pad;
+    for (int64_t b0 = 0; b0 < psi_pad; b0 += bucket) {
+        const int64_t b1 = (psi_pad - b0 > bucket) ? b0 + bucket : psi_pad;
+        if ((rc = plan_bucket(&plan, b0, b1, nullptr, stream)) != ZERO_OK) return rc;
+    }
+    return plan_end(&plan, result, stream);
+}
+
+}  // namespace
+
+extern "C" size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp,
+                                       int32_t in_place) {
+    if (psi_pad < 0 || hp == nullptr) return 0;
+    return workspace_bytes(psi_pad, hp, in_place != 0);
+}
+
+extern "C" int zero_step(const void* const* grads, int32_t grad_dtype, float* master, float* m,
+                         float* v, uint16_t* w_bf16, int64_t psi_pad, int32_t N,
+                         const zero_adam_hparams* hp, float loss_scale, void* workspace,
+                         size_t workspace_bytes_given, zero_step_result* result, void* stream) {
+    if (master == nullptr && psi_pad > 0) return ZERO_ERR_ARG;
+    return run_step(grads, grad_dtype, master, m, v, w_bf16, master, m, v, w_bf16, psi_pad, N, hp,
+                    loss_scale, workspace, workspace_bytes_given, result, stream);
+}
+
+extern "C" int zero_step_into(const void* const* grads, int32_t grad_dtype,
+                              const float* src_master, const float* src_m, const float* src_v,
+                              const uint16_t* src_w_bf16, float* dst_master, float* dst_m,
+                              float* dst_v, uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
+                              const zero_adam_hparams* hp, float loss_scale, void* workspace,
+                              size_t workspace_bytes_given, zero_step_result* result,
+                              void* stream) {
+    if (psi_pad > 0 && (src_master == nullptr || dst_master == nullptr)) return ZERO_ERR_ARG;
+    if (psi_pad > 0 && static_cast<const void*>(src_master) == static_cast<const void*>(dst_master))
+        return ZERO_ERR_OVERLAP;
+    return run_step(grads, grad_dtype, src_master, src_m, src_v, src_w_bf16, dst_master, dst_m,
+                    dst_v, dst_w_bf16, psi_pad, N, hp, loss_scale, workspace,
+                    workspace_bytes_given, result, stream);
+}
+
+extern "C" int zero_plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
+                              const float* src_master, const float* src_m, const float* src_v,
+                              const uint16_t* src_w_bf16, float* dst_master, float* dst_m,
+                              float* dst_v, uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
+                              const zero_adam_hparams* hp, float loss_scale, void* workspace,
+                              size_t workspace_bytes_given) {
+    if (psi_pad > 0 && (src_master == nullptr || dst_master == nullptr)) return ZERO_ERR_ARG;
+    return plan_init(plan, grads, grad_dtype, src_master, src_m, src_v, src_w_bf16, dst_master,
+                     dst_m, dst_v, dst_w_bf16, psi_pad, N, hp, loss_scale, workspace,
+                     workspace_bytes_given, true);
+}
+
+extern "C" int zero_plan_begin(zero_plan* plan, void* stream) { return plan_begin(plan, stream); }
+
+extern "C" int zero_plan_bucket(zero_plan* plan, int64_t begin, int64_t end,
+                                const void* const* bucket_grads, void* stream) {
+    return plan_bucket(plan, begin, end, bucket_grads, stream);
+}
+
+extern "C" int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream) {
+    return plan_end(plan, result, stream);
+}
+
+extern "C" uint64_t zero_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -1,0 +1,219 @@
+"""Host-side bookkeeping around the C-ABI step.
+
+The C ABI leaves the step counter and the loss scale to the caller.  This
+module keeps them:
+  - the Adam step t advances only on applied steps;
+  - a dynamic loss scale halves after an overflowing (skipped) step and
+    doubles after ``growth_interval`` clean steps in a row.
+It also owns the device buffers of one simulated data-parallel group, all
+allocated with torch:
+  - N gradient buffers;
+  - the FP32 master/m/v and the BF16 working weights;
+  - a second set of those when the step runs out of place;
+  - the workspace, and a pinned result word the device writes.
+Every step runs in libzero_gb300.so; nothing here touches the data.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import zero as Z
+
+
+@dataclass
+class LossScaler:
+    """Dynamic loss scale: scale *= backoff after a step with a non-finite
+    gradient (the clean-step count restarts), scale *= growth after
+    ``interval`` clean steps in a row.  A static scale never changes."""
+    scale: float = 1.0
+    dynamic: bool = False
+    interval: int = 2000
+    backoff: float = 0.5
+    growth: float = 2.0
+    good_steps: int = 0
+
+    def update(self, found_nonfinite: bool) -> None:
+        if not self.dynamic:
+            return
+        if found_nonfinite:
+            self.scale *= self.backoff
+            self.good_steps = 0
+            return
+        self.good_steps += 1
+        if self.good_steps == self.interval:
+            self.scale *= self.growth
+            self.good_steps = 0
+
+
+class ZeroAdam:
+    """The N simulated ranks' update state on one GPU, stepped through the C ABI.
+
+    ``out_of_place`` keeps two sets of master/m/v/w and calls
+    ``zero_step_into`` (the post-step state lands in the other set, which
+    then becomes current).  Otherwise ``zero_step`` updates one set in place.
+    """
+
+    def __init__(self, psi_pad: int, N: int, grad_dtype: str = "bf16", *, lr=1e-3, beta1=0.9,
+                 beta2=0.999, eps=1e-8, weight_decay=0.0, max_grad_norm=0.0,
+                 skip_on_overflow=False, bucket_elems=0, loss_scale=1.0,
+                 dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
+                 device="cuda", master: torch.Tensor | None = None):
+        self.psi_pad, self.N = psi_pad, N
+        self.grad_dtype = Z.ZERO_GRAD_BF16 if grad_dtype == "bf16" else Z.ZERO_GRAD_FP32
+        self.hp = Z.make_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1,
+                                 skip_on_overflow, bucket_elems)
+        self.t = 0  # applied steps so far
+        self.scaler = LossScaler(loss_scale, dynamic_loss_scale, growth_interval)
+        self.out_of_place = out_of_place
+        self.device = torch.device(device)
+        sets = 2 if out_of_place else 1
+        self._bufs = []
+        for k in range(sets):
+            p = (master.clone() if master is not None else
+                 torch.zeros(psi_pad, dtype=torch.float32, device=self.device))
+            self._bufs.append({
+                "master": p,
+                "m": torch.zeros(psi_pad, dtype=torch.float32, device=self.device),
+                "v": torch.zeros(psi_pad, dtype=torch.float32, device=self.device),
+                "w": torch.zeros(psi_pad, dtype=torch.int16, device=self.device),
+            })
+        self.cur = 0
+        self.ws_bytes = Z.zero_workspace_bytes(psi_pad, self.hp, not out_of_place)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.result_t = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+        self.last = None
+
+    # ---------------------------------------------------------------- state
+    def state(self) -> dict:
+        """The current master/m/v (FP32) and working weights (BF16 bits as int16)."""
+        return self._bufs[self.cur]
+
+    def load_state(self, master, m, v, w) -> None:
+        s = self.state()
+        s["master"].copy_(master)
+        s["m"].copy_(m)
+        s["v"].copy_(v)
+        s["w"].copy_(w)
+
+    # ---------------------------------------------------------------- step
+    def enqueue(self, grads, stream=None, api: str = "step", bucket_events=None) -> int:
+        """Enqueue one step on ``stream`` (torch's current stream by default)
+        without waiting for it.  Returns the C status (ZERO_OK on success).
+
+        api="step" calls zero_step / zero_step_into.  api="plan" enqueues the
+        same kernels bucket by bucket through the plan entry points.  Then
+        ``bucket_events``, a list of (start, end) torch CUDA events, one pair
+        per bucket, is recorded around each bucket's first-pass launch."""
+        self.hp.step = self.t + 1
+        src = self._bufs[self.cur]
+        if api == "plan":
+            return self._enqueue_plan(grads, src, stream, bucket_events)
+        if self.out_of_place:
+            dst = self._bufs[1 - self.cur]
+            rc = Z.zero_step_into(grads, self.grad_dtype, src["master"], src["m"], src["v"],
+                                  src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
+                                  self.psi_pad, self.N, self.hp, self.scaler.scale,
+                                  self.workspace, self.ws_bytes, self.result_t, stream)
+        else:
+            rc = Z.zero_step(grads, self.grad_dtype, src["master"], src["m"], src["v"], src["w"],
+                             self.psi_pad, self.N, self.hp, self.scaler.scale, self.workspace,
+                             self.ws_bytes, self.result_t, stream)
+        Z.check(rc, "zero_step")
+        if self.out_of_place:
+            self.cur = 1 - self.cur  # dst always holds the post-step state
+        return rc
+
+    def bucket_bounds(self) -> list[tuple[int, int]]:
+        b = self.hp.bucket_elems or self.psi_pad
+        return [(b0, min(self.psi_pad, b0 + b)) for b0 in range(0, self.psi_pad, b)]
+
+    def _enqueue_plan(self, grads, src, stream, bucket_events) -> int:
+        dst = self._bufs[1 - self.cur] if self.out_of_place else src
+        plan = Z.zero_plan()
+        Z.check(Z.zero_plan_init(plan, grads, self.grad_dtype, src["master"], src["m"], src["v"],
+                                 src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
+                                 self.psi_pad, self.N, self.hp, self.scaler.scale, self.workspace,
+                                 self.ws_bytes), "zero_plan_init")
+        Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        for k, (b0, b1) in enumerate(self.bucket_bounds()):
+            if bucket_events is not None:
+                bucket_events[k][0].record(s)
+            Z.check(Z.zero_plan_bucket(plan, b0, b1, None, stream), "zero_plan_bucket")
+            if bucket_events is not None:
+                bucket_events[k][1].record(s)
+        rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
+        if self.out_of_place:
+            self.cur = 1 - self.cur
+        return rc
+
+    # ---------------------------------------------------------------- host gradients
+    def make_slots(self, bucket_elems: int | None = None) -> list[list[torch.Tensor]]:
+        """Two device staging slots, each holding one bucket of all N ranks'
+        gradients: the two-buffer pattern (one slot in use, one loading)."""
+        b = bucket_elems or self.hp.bucket_elems or self.psi_pad
+        dt = torch.bfloat16 if self.grad_dtype == Z.ZERO_GRAD_BF16 else torch.float32
+        return [[torch.empty(b, dtype=dt, device=self.device) for _ in range(self.N)]
+                for _ in range(2)]
+
+    def enqueue_from_host(self, host_grads, slots, copy_stream, stream=None) -> int:
+        """Enqueue one step whose N gradients sit in pinned host memory.  Bucket
+        k is copied into slot k % 2 on ``copy_stream`` while the compute stream
+        reduces bucket k - 1 from the other slot.  A slot is refilled only once
+        the bucket that used it has been read."""
+        self.hp.step = self.t + 1
+        src = self._bufs[self.cur]
+        dst = self._bufs[1 - self.cur] if self.out_of_place else src
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        plan = Z.zero_plan()
+        Z.check(Z.zero_plan_init(plan, [None] * self.N, self.grad_dtype, src["master"], src["m"],
+                                 src["v"], src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
+                                 self.psi_pad, self.N, self.hp, self.scaler.scale,
+                                 self.workspace, self.ws_bytes), "zero_plan_init")
+        Z.check(Z.zero_plan_begin(plan, s), "zero_plan_begin")
+        if not hasattr(self, "_slot_events"):
+            # freed[k] is recorded after the last read of slot k, also across steps
+            self._slot_events = ([torch.cuda.Event(), torch.cuda.Event()],
+                                 [torch.cuda.Event(), torch.cuda.Event()])
+        loaded, freed = self._slot_events
+        b = slots[0][0].numel()
+        for k, b0 in enumerate(range(0, self.psi_pad, b)):
+            b1 = min(self.psi_pad, b0 + b)
+            slot = slots[k % 2]
+            copy_stream.wait_event(freed[k % 2])  # no-op before the first record
+            with torch.cuda.stream(copy_stream):
+                for i in range(self.N):
+                    slot[i][:b1 - b0].copy_(host_grads[i][b0:b1], non_blocking=True)
+            loaded[k % 2].record(copy_stream)
+            s.wait_event(loaded[k % 2])
+            Z.check(Z.zero_plan_bucket(plan, b0, b1, slot, s), "zero_plan_bucket")
+            freed[k % 2].record(s)
+        rc = Z.check(Z.zero_plan_end(plan, self.result_t, s), "zero_plan_end")
+        if self.out_of_place:
+            self.cur = 1 - self.cur
+        return rc
+
+    def finish(self, stream=None) -> dict:
+        """Wait for the last enqueued step, read its result and advance the
+        host bookkeeping (t and the loss scale)."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        s.synchronize()
+        raw = self.result_t.clone()
+        status = int(raw[0])
+        found = bool(int(raw[1]))
+        norm = float(raw[2:3].view(torch.float32)[0])
+        coef = float(raw[3:4].view(torch.float32)[0])
+        Z.check(status, "zero_step (device)")
+        applied = status == Z.ZERO_OK
+        if applied:
+            self.t += 1
+        self.scaler.update(found)
+        self.last = {"applied": applied, "found_nonfinite": found, "grad_norm": norm,
+                     "clip_coef": coef, "status": status}
+        return self.last
+
+    def step(self, grads, stream=None, api: str = "step", bucket_events=None) -> dict:
+        self.enqueue(grads, stream, api, bucket_events)
+        return self.finish(stream)
