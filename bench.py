@@ -67,7 +67,20 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 10)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--psi", type=int, default=0,
+                    help="reduced parameter count of the same workload (profiling captures "
+                         "only; the benchmark line is the full size)")
     return ap.parse_args(argv)
+
+
+def select_workload(args):
+    import dataclasses
+    from zero_sharded_mixed_04_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.psi:
+        wl = dataclasses.replace(wl, name=f"{wl.name}[psi={args.psi}]", psi_flat=args.psi,
+                                 tensor_sizes=())
+    return wl
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -249,7 +262,7 @@ def run_ours(args, world, rank, local):
     group = Group(world)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = synth.WORKLOADS[args.workload]
+    wl = select_workload(args)
     out_of_place = not args.in_place
     grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
     master = synth.make_master(wl, dev)
@@ -402,7 +415,7 @@ def run_reference(args, world, rank):
     import torch
     import oracle
     from zero_sharded_mixed_04_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
+    wl = select_workload(args)
     oracle.build()
     unit = wl.N * 128
     # size each step's sample so the whole run takes about a minute
