@@ -73,7 +73,9 @@ typedef enum {
     ZERO_ERR_CUDA = -3,       /* a CUDA call failed while enqueueing               */
     ZERO_ERR_TIMEOUT = -4,    /* a bounded wait inside a kernel gave up            */
     ZERO_ERR_WORKSPACE = -5,  /* workspace missing, too small or misaligned        */
-    ZERO_ERR_OVERLAP = -6     /* two buffers that must be disjoint overlap         */
+    ZERO_ERR_OVERLAP = -6,    /* two buffers that must be disjoint overlap         */
+    ZERO_ERR_TOO_LARGE = -7   /* the step needs more scratch than zero_step_noalloc's
+                                 fixed array holds                                 */
 } zero_status;
 
 typedef enum {
@@ -306,6 +308,40 @@ const char* zero_status_str(int status);
 /* Number of kernels this library has launched in this process.  Host only,
  * monotonic, thread-safe.  Memsets and copies are not counted. */
 uint64_t zero_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * zero_step without a caller-provided workspace.  The pages have no
+ * counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory themselves.  Examples: a host program whose device
+ * memory is owned by another allocator or memory pool, a plugin inside a
+ * framework that hands it only the tensors it works on, or a control loop
+ * where an allocation's implicit device synchronisation is not acceptable.
+ *
+ * It is the in-place zero_step, with the same arguments, checks, arithmetic
+ * and results.  The workspace is a fixed array of ZERO_NOALLOC_SCRATCH_BYTES
+ * in device memory, defined inside this library.  Every GPU that loads the
+ * library holds that array until the process exits.  The one-pass form (no
+ * clipping, no skip_on_overflow) fits at any size.  The two-pass form (with
+ * clipping or skip_on_overflow) also keeps the FP32 combined gradient there,
+ * so it accepts psi_pad up to ZERO_NOALLOC_MAX_TWO_PASS_ELEMS.  Larger
+ * requests return ZERO_ERR_TOO_LARGE before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address, with that
+ * device current, and keeps it for later calls.  Make that first call before
+ * any stream capture.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  It clears, on `stream`, the part
+ * of the array each step must start from zero.
+ *
+ * All calls on a device share the one array, which keeps the last step's
+ * contents.  Two calls whose work overlaps on the GPU race on it: from
+ * different streams or host threads, order them (one stream, or events)
+ * yourself.  Returns as zero_step does, or ZERO_ERR_TOO_LARGE. */
+#define ZERO_NOALLOC_MAX_TWO_PASS_ELEMS 4194304
+#define ZERO_NOALLOC_SCRATCH_BYTES (16640 + 4 * ZERO_NOALLOC_MAX_TWO_PASS_ELEMS)
+int zero_step_noalloc(const void* const* grads, int32_t grad_dtype,
+                      float* master, float* m, float* v, uint16_t* w_bf16,
+                      int64_t psi_pad, int32_t N, const zero_adam_hparams* hp, float loss_scale,
+                      zero_step_result* result, void* stream);
 
 #ifdef __cplusplus
 }

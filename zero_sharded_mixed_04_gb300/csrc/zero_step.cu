@@ -779,3 +779,54 @@ extern "C" int zero_plan_end(zero_plan* plan, zero_step_result* result, void* st
 }
 
 extern "C" uint64_t zero_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// ------------------------------------------------------------------ no-allocation entry point
+//
+// For callers that cannot allocate device memory: zero_step with its
+// workspace in a fixed array defined here.  The array lives in every GPU that
+// loads this library until the process exits.  Host code must not pass the
+// array's name to a kernel.  On the host that name stands for a host-side
+// copy, so the address a kernel may use is looked up per device below.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ZERO_NOALLOC_SCRATCH_BYTES];
+static_assert(ZERO_NOALLOC_SCRATCH_BYTES == kGradOffset + 4 * ZERO_NOALLOC_MAX_TWO_PASS_ELEMS,
+              "header size of the no-allocation scratch");
+
+namespace {
+
+constexpr int kMaxDevices = 256;
+
+// Device address of g_noalloc_scratch on the current device.  It is looked
+// up on the first call per device, with that device current, and then
+// cached.  Returns nullptr if the lookup fails.
+void* noalloc_scratch(int device) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[device] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();  // leave no error behind for the caller's next call
+            return nullptr;
+        }
+        addr[device] = p;
+    }
+    return addr[device];
+}
+
+}  // namespace
+
+extern "C" int zero_step_noalloc(const void* const* grads, int32_t grad_dtype, float* master,
+                                 float* m, float* v, uint16_t* w_bf16, int64_t psi_pad, int32_t N,
+                                 const zero_adam_hparams* hp, float loss_scale,
+                                 zero_step_result* result, void* stream) {
+    if (hp == nullptr || psi_pad < 0) return ZERO_ERR_ARG;
+    if (workspace_bytes(psi_pad, hp, true) > ZERO_NOALLOC_SCRATCH_BYTES) return ZERO_ERR_TOO_LARGE;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
+    void* scratch = noalloc_scratch(device);
+    if (scratch == nullptr) return ZERO_ERR_CUDA;
+    return zero_step(grads, grad_dtype, master, m, v, w_bf16, psi_pad, N, hp, loss_scale, scratch,
+                     ZERO_NOALLOC_SCRATCH_BYTES, result, stream);
+}

@@ -38,6 +38,10 @@ ZERO_ERR_CUDA = -3
 ZERO_ERR_TIMEOUT = -4
 ZERO_ERR_WORKSPACE = -5
 ZERO_ERR_OVERLAP = -6
+ZERO_ERR_TOO_LARGE = -7
+
+ZERO_NOALLOC_MAX_TWO_PASS_ELEMS = 4194304
+ZERO_NOALLOC_SCRATCH_BYTES = 16640 + 4 * ZERO_NOALLOC_MAX_TWO_PASS_ELEMS
 
 ZERO_GRAD_BF16 = 0
 ZERO_GRAD_FP32 = 1
@@ -101,6 +105,9 @@ _lib.zero_plan_bucket.argtypes = [_PLAN, _i64, _i64, _P, _P]
 _lib.zero_plan_bucket.restype = ctypes.c_int
 _lib.zero_plan_end.argtypes = [_PLAN, _P, _P]
 _lib.zero_plan_end.restype = ctypes.c_int
+_lib.zero_step_noalloc.argtypes = [_P, _i32, _P, _P, _P, _P, _i64, _i32,
+                                   ctypes.POINTER(zero_adam_hparams), _f32, _P, _P]
+_lib.zero_step_noalloc.restype = ctypes.c_int
 _lib.zero_ledger.argtypes = [_i64, _i32, _i32, _i32, _i32]
 _lib.zero_ledger.restype = _i64
 _lib.zero_comm_volume.argtypes = [_i64, _i32, _i32]
@@ -222,6 +229,16 @@ def zero_plan_end(plan: zero_plan, result=None, stream=None) -> int:
     return _lib.zero_plan_end(ctypes.byref(plan), _addr(result), _stream(stream))
 
 
+def zero_step_noalloc(grads, grad_dtype: int, master, m, v, w_bf16, psi_pad: int, N: int,
+                      hp: zero_adam_hparams, loss_scale: float, result=None,
+                      stream=None) -> int:
+    """zero_step with the library's fixed scratch array as its workspace, for
+    callers that cannot allocate device memory (see include/zero_gb300.h)."""
+    return _lib.zero_step_noalloc(_grad_array(grads), grad_dtype, _addr(master), _addr(m),
+                                  _addr(v), _addr(w_bf16), psi_pad, N, ctypes.byref(hp),
+                                  loss_scale, _addr(result), _stream(stream))
+
+
 def zero_ledger(psi: int, N: int, stage: int, grad_bytes: int = 2, optim_bytes: int = 12) -> int:
     return _lib.zero_ledger(psi, N, stage, grad_bytes, optim_bytes)
 
@@ -243,4 +260,4 @@ def exported_symbols() -> list[str]:
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
             "zero_step_into", "zero_plan_init", "zero_plan_begin", "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
-            "zero_launch_count"]
+            "zero_launch_count", "zero_step_noalloc"]
