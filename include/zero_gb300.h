@@ -246,6 +246,15 @@ typedef struct {
     int32_t in_place;
     int32_t two_pass;                  /* 1 if the update waits for a second pass          */
     int32_t state;                     /* 0 unset, 1 initialised, 2 begun                 */
+    int32_t overlap_buckets;           /* 0 (as zero_plan_init leaves it): every bucket
+                                          launch waits for all work before it on the
+                                          stream.  1: the caller promises to enqueue
+                                          nothing on the stream between this plan's
+                                          zero_plan_bucket calls, so consecutive bucket
+                                          launches may overlap (one starts while the
+                                          previous drains), as zero_step runs them.
+                                          Buckets read through bucket_grads never
+                                          overlap.                                        */
 } zero_plan;
 
 /* Fills *plan from the arguments of zero_step (dst == src) or zero_step_into

@@ -48,7 +48,7 @@ def _np(t):
 def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, wd=0.0,
                clip=0.0, skip=False, out_of_place=False, bucket=0, loss_scale=1.0,
                dynamic=False, growth_interval=2000, sigma=1e-3, bad_step=0, bad_value=np.inf,
-               seed=1234, api="step"):
+               seed=1234, api="step", per_bucket_events=False):
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     unit = N * 128
@@ -69,7 +69,11 @@ def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, 
         grads = _make_grads(N, psi, psi_pad, dtype, sigma * o_scale, seed + step)
         if step == bad_step and psi > 0:
             grads[N - 1][min(psi - 1, 12345)] = float(bad_value)
-        res = opt.step([g.to(dev) for g in grads], api=api)
+        ev = None
+        if per_bucket_events:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in opt.bucket_bounds()]
+        res = opt.step([g.to(dev) for g in grads], api=api, bucket_events=ev)
         ores = oracle_mod.zero_step([_np(g) for g in grads], ref["master"], ref["m"], ref["v"],
                                     ref["w"], hp, o_t + 1, o_scale, skip)
         compare_result(res, ores)
@@ -197,11 +201,15 @@ def test_launch_count_grows(zero_lib):
 
 @pytest.mark.parametrize("out_of_place,skip,clip", [(False, False, 0.0), (True, True, 0.0),
                                                    (False, True, 0.0), (True, False, 0.3)])
-def test_plan_api(zero_lib, oracle_mod, out_of_place, skip, clip):
-    """The bucketed entry points give the same result as zero_step."""
+@pytest.mark.parametrize("per_bucket_events", [False, True])
+def test_plan_api(zero_lib, oracle_mod, out_of_place, skip, clip, per_bucket_events):
+    """The bucketed entry points give the same result as zero_step, with
+    consecutive bucket launches overlapping (nothing enqueued between them)
+    and without (events recorded between them)."""
     run_parity(zero_lib, oracle_mod, N=8, psi=PSI_MULTI_SWEEP, bucket=400_000,
                out_of_place=out_of_place, skip=skip, clip=clip, steps=3, api="plan",
-               bad_step=2 if skip else 0, loss_scale=4096.0, dynamic=skip)
+               bad_step=2 if skip else 0, loss_scale=4096.0, dynamic=skip,
+               per_bucket_events=per_bucket_events)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])

@@ -209,6 +209,19 @@ __device__ __forceinline__ void store_w8(uint16_t* base, int64_t j, const float 
     __stcs(reinterpret_cast<uint4*>(base + j), packed);
 }
 
+// Programmatic dependent launch.  Consecutive bucket launches of one step
+// touch disjoint elements, so launch k+1 may start streaming while launch k
+// drains.  Every CTA allows the next launch to be scheduled as soon as it
+// starts.  The one write that needs ordering (the CTA's norm slot) waits for
+// the previous grid to complete.  The next grid's CTAs can only be scheduled
+// once every CTA of this grid is resident, so that wait always ends.
+__device__ __forceinline__ void allow_next_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // End of a CTA's share: publish the overflow flag (one atomic per warp that
 // saw a non-finite value) and add the CTA's sum of squares to its FP64 slot.
 // Warp-shuffle tree, then the warps in order, so the sum is deterministic.
@@ -223,7 +236,12 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
         double t = 0.0;
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w) t += warp_sum[w];
-        a.partials[blockIdx.x] += t;  // launches of one step are ordered on one stream
+        // A bucket launch may start while the previous one drains (programmatic
+        // dependent launch).  Its slot update must still come after the
+        // previous launch's: wait for that grid to complete first.  Without a
+        // programmatic launch this returns at once.
+        grid_dependency_wait();
+        a.partials[blockIdx.x] += t;
     }
 }
 
@@ -231,32 +249,59 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 
 // One pass: reduce-scatter + scale + check + Adam + BF16 all-gather.  Reads
 // src_*, writes dst_* (the same arrays for an in-place step).
-template <int NT, bool kBF16>
-__global__ void __launch_bounds__(kThreads) zero_fused_kernel(const __grid_constant__ StepArgs a) {
-    unsigned bad = 0;
-    double sumsq = 0.0;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
-         q += stride) {
-        const int64_t j = a.begin + q * kVec;
-        float p[kVec], m[kVec], v[kVec], g[kVec];
-        load8(a.src_master, j, p);
-        load8(a.src_m, j, m);
-        load8(a.src_v, j, v);
-        combine<NT, kBF16>(a, j, g);
+// One 8-element group: reduce-scatter + scale + check + Adam + BF16 all-gather.
+template <int NT, bool kBF16, int U>
+__device__ __forceinline__ void fused_groups(const StepArgs& a, const int64_t (&j)[U],
+                                             unsigned& bad, double& sumsq) {
+    float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
+    // every load of the U groups is issued before any arithmetic
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        load8(a.src_master, j[u], p[u]);
+        load8(a.src_m, j[u], m[u]);
+        load8(a.src_v, j[u], v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
         float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-            const float gs = __fmul_rn(g[e], a.s.inv);
+            const float gs = __fmul_rn(g[u][e], a.s.inv);
             bad |= is_nonfinite(gs) ? 1u : 0u;
             sq = fmaf(gs, gs, sq);
-            adam_element(gs, p[e], m[e], v[e], a.s);
+            adam_element(gs, p[u][e], m[u][e], v[u][e], a.s);
         }
         sumsq += static_cast<double>(sq);
-        store8(a.dst_master, j, p);
-        store8(a.dst_m, j, m);
-        store8(a.dst_v, j, v);
-        store_w8(a.dst_w, j, p);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        store8(a.dst_master, j[u], p[u]);
+        store8(a.dst_m, j[u], m[u]);
+        store8(a.dst_v, j[u], v[u]);
+        store_w8(a.dst_w, j[u], p[u]);
+    }
+}
+
+// One pass: reduce-scatter + scale + check + Adam + BF16 all-gather.  Reads
+// src_*, writes dst_* (the same arrays for an in-place step).  Each thread
+// keeps two groups (a grid stride apart) in flight: with 128 registers and two
+// CTAs per SM that measured faster than one group at 64 registers and four.
+template <int NT, bool kBF16>
+__global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_constant__ StepArgs a) {
+    allow_next_launch();
+    unsigned bad = 0;
+    double sumsq = 0.0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (; q + stride < a.n8; q += 2 * stride) {
+        const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+        fused_groups<NT, kBF16, 2>(a, j, bad, sumsq);
+    }
+    if (q < a.n8) {
+        const int64_t j[1] = {a.begin + q * kVec};
+        fused_groups<NT, kBF16, 1>(a, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -265,6 +310,7 @@ __global__ void __launch_bounds__(kThreads) zero_fused_kernel(const __grid_const
 // FP32 combined gradient to the workspace.
 template <int NT, bool kBF16>
 __global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_constant__ StepArgs a) {
+    allow_next_launch();
     unsigned bad = 0;
     double sumsq = 0.0;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
@@ -437,9 +483,28 @@ int grid_for(const void* fn, int device, int64_t n8) {
     return g < 1 ? 1 : static_cast<int>(g);
 }
 
-bool launch(StepKernel fn, int device, const StepArgs& a, cudaStream_t stream) {
+// Launches fn over a.n8 groups.  With overlap_previous the launch may begin
+// while the kernel before it on the stream drains (programmatic dependent
+// launch); only first-pass bucket launches of one step, whose elements are
+// disjoint from the previous bucket's, ask for it.
+bool launch(StepKernel fn, int device, const StepArgs& a, cudaStream_t stream,
+            bool overlap_previous = false) {
     const int grid = grid_for(reinterpret_cast<const void*>(fn), device, a.n8);
-    fn<<<grid, kThreads, 0, stream>>>(a);
+    if (overlap_previous) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fn, a) != cudaSuccess) return false;
+    } else {
+        fn<<<grid, kThreads, 0, stream>>>(a);
+    }
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError() == cudaSuccess;
 }
@@ -655,7 +720,13 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     a.n8 = (end - begin) / kVec;
     const bool bf16 = p->grad_dtype == ZERO_GRAD_BF16;
     const StepKernel fn = p->two_pass ? pick<ReduceK>(p->N, bf16) : pick<FusedK>(p->N, bf16);
-    if (!launch(fn, device, a, static_cast<cudaStream_t>(stream))) return ZERO_ERR_CUDA;
+    // Overlap with the previous bucket only when that launch is the one right
+    // before this on the stream.  The caller promises that by setting
+    // overlap_buckets; zero_step does.  A bucket read from a staging slot
+    // follows the wait for that slot's copy, so it is launched in plain
+    // stream order.
+    const bool overlap = p->overlap_buckets != 0 && begin > 0 && bucket_grads == nullptr;
+    if (!launch(fn, device, a, static_cast<cudaStream_t>(stream), overlap)) return ZERO_ERR_CUDA;
     p->cursor = end;
     return ZERO_OK;
 }
@@ -714,6 +785,7 @@ int run_step(const void* const* grads, int32_t grad_dtype, const float* src_mast
                        dst_v, dst_w, psi_pad, N, hp, loss_scale, workspace, workspace_bytes_given,
                        false);
     if (rc != ZERO_OK) return rc;
+    plan.overlap_buckets = 1;  // the buckets below are launched back to back
     if ((rc = plan_begin(&plan, stream)) != ZERO_OK) return rc;
     const int64_t bucket = hp->bucket_elems > 0 ? hp->bucket_elems : psi_pad;
     for (int64_t b0 = 0; b0 < psi_pad; b0 += bucket) {

@@ -98,18 +98,23 @@ class ZeroAdam:
         s["w"].copy_(w)
 
     # ---------------------------------------------------------------- step
-    def enqueue(self, grads, stream=None, api: str = "step", bucket_events=None) -> int:
+    def enqueue(self, grads, stream=None, api: str = "step", bucket_events=None,
+                span_events=None) -> int:
         """Enqueue one step on ``stream`` (torch's current stream by default)
         without waiting for it.  Returns the C status (ZERO_OK on success).
 
         api="step" calls zero_step / zero_step_into.  api="plan" enqueues the
-        same kernels bucket by bucket through the plan entry points.  Then
-        ``bucket_events``, a list of (start, end) torch CUDA events, one pair
-        per bucket, is recorded around each bucket's first-pass launch."""
+        same kernels bucket by bucket through the plan entry points:
+          - ``span_events``, a (start, end) pair of torch CUDA events, is
+            recorded before the first and after the last bucket launch.
+            Consecutive launches still overlap, as in zero_step.
+          - ``bucket_events``, one (start, end) pair per bucket, is recorded
+            around each bucket's launch instead.  The events between launches
+            keep them from overlapping."""
         self.hp.step = self.t + 1
         src = self._bufs[self.cur]
         if api == "plan":
-            return self._enqueue_plan(grads, src, stream, bucket_events)
+            return self._enqueue_plan(grads, src, stream, bucket_events, span_events)
         if self.out_of_place:
             dst = self._bufs[1 - self.cur]
             rc = Z.zero_step_into(grads, self.grad_dtype, src["master"], src["m"], src["v"],
@@ -129,21 +134,28 @@ class ZeroAdam:
         b = self.hp.bucket_elems or self.psi_pad
         return [(b0, min(self.psi_pad, b0 + b)) for b0 in range(0, self.psi_pad, b)]
 
-    def _enqueue_plan(self, grads, src, stream, bucket_events) -> int:
+    def _enqueue_plan(self, grads, src, stream, bucket_events, span_events=None) -> int:
         dst = self._bufs[1 - self.cur] if self.out_of_place else src
         plan = Z.zero_plan()
         Z.check(Z.zero_plan_init(plan, grads, self.grad_dtype, src["master"], src["m"], src["v"],
                                  src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
                                  self.psi_pad, self.N, self.hp, self.scaler.scale, self.workspace,
                                  self.ws_bytes), "zero_plan_init")
+        # nothing but bucket launches goes between the buckets unless events
+        # are recorded around each one
+        plan.overlap_buckets = 0 if bucket_events is not None else 1
         Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if span_events is not None:
+            span_events[0].record(s)
         for k, (b0, b1) in enumerate(self.bucket_bounds()):
             if bucket_events is not None:
                 bucket_events[k][0].record(s)
             Z.check(Z.zero_plan_bucket(plan, b0, b1, None, stream), "zero_plan_bucket")
             if bucket_events is not None:
                 bucket_events[k][1].record(s)
+        if span_events is not None:
+            span_events[1].record(s)
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
         if self.out_of_place:
             self.cur = 1 - self.cur
@@ -214,6 +226,7 @@ class ZeroAdam:
                      "clip_coef": coef, "status": status}
         return self.last
 
-    def step(self, grads, stream=None, api: str = "step", bucket_events=None) -> dict:
-        self.enqueue(grads, stream, api, bucket_events)
+    def step(self, grads, stream=None, api: str = "step", bucket_events=None,
+             span_events=None) -> dict:
+        self.enqueue(grads, stream, api, bucket_events, span_events)
         return self.finish(stream)

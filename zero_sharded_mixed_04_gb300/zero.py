@@ -75,7 +75,7 @@ class zero_plan(ctypes.Structure):
                 ("cursor", ctypes.c_int64), ("hp", zero_adam_hparams),
                 ("loss_scale", ctypes.c_float), ("grad_dtype", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("in_place", ctypes.c_int32), ("two_pass", ctypes.c_int32),
-                ("state", ctypes.c_int32)]
+                ("state", ctypes.c_int32), ("overlap_buckets", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
