@@ -265,6 +265,9 @@ def run_ours(args, world, rank, local):
     wl = select_workload(args)
     out_of_place = not args.in_place
     grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
+    # the end-to-end leg's pinned host copy of the gradients, made before the
+    # large device allocations as an application would hold it from the start
+    host_grads = None if args.no_e2e else pin_host_grads(grads)
     master = synth.make_master(wl, dev)
     opt = ZeroAdam(wl.psi_pad, wl.N, wl.grad_dtype, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
                    eps=wl.eps, weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm,
@@ -339,7 +342,7 @@ def run_ours(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, opt, grads, wl, stream, dev, group)
+        e2e = run_e2e(args, opt, grads, host_grads, wl, stream, dev, group)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -375,24 +378,38 @@ def run_ours(args, world, rank, local):
     group.close()
 
 
-def run_e2e(args, opt, grads, wl, stream, dev, group) -> dict:
-    """The same step through the public API with the gradients in pinned host
-    memory: every step copies them host-to-device through two bucket slots
-    (overlapped with the reduction of the previous bucket) and reads the
-    step result back to the host."""
+def pin_host_grads(grads):
+    """The gradients in one pinned host allocation (the pinned allocator rounds
+    each allocation up to a power of two, so one buffer holds every rank)."""
     import torch
-    # one pinned allocation for all ranks (the pinned allocator rounds each
-    # allocation up to a power of two)
     n = grads[0].numel()
     flat = torch.empty(n * len(grads), dtype=grads[0].dtype, pin_memory=True)
     host = [flat[i * n:(i + 1) * n] for i in range(len(grads))]
     for h, g in zip(host, grads):
         h.copy_(g)
+    return flat, host
+
+
+def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
+    """The same step through the public API with the gradients in pinned host
+    memory: every step copies them host-to-device through two bucket slots
+    (overlapped with the reduction of the previous bucket) and reads the
+    step result back to the host."""
+    import torch
+    flat, host = host_grads
     slots = opt.make_slots()
     copy_stream = torch.cuda.Stream(dev)
     steps = args.e2e_steps or max(1, min(args.steps, 10))
     opt.enqueue_from_host(host, slots, copy_stream, stream)  # one untimed warm-up step
     opt.finish(stream)
+    # the host link on its own: every rank's gradient copied host-to-device
+    # into the device-resident gradient buffers, once
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for h, g in zip(host, grads):
+        g.copy_(h, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    link_gbs = sum(h.numel() * h.element_size() for h in host) / (time.perf_counter() - t0) / 1e9
     group.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -405,9 +422,11 @@ def run_e2e(args, opt, grads, wl, stream, dev, group) -> dict:
     dt = (time.perf_counter() - t0) / steps
     dt = group.max(dt)
     h2d = sum(g.numel() * g.element_size() for g in grads)
-    del host, slots, flat
+    del host, slots, flat, host_grads
     return {"value": round(group.sum(float(wl.psi)) / dt, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16, "ms_per_step": round(dt * 1e3, 3),
+            "h2d_link_gbs": round(link_gbs, 1),
+            "h2d_link_bound_ms": round(h2d / (link_gbs * 1e9) * 1e3, 3),
             "path": "pinned host grads -> two device bucket slots -> zero_plan_bucket; "
                     "result read by the host"}
 

@@ -353,30 +353,34 @@ __device__ __forceinline__ void copy_state(const StepArgs& a) {
 // workspace's combined gradient, unless the step was skipped.  A skipped
 // out-of-place step copies src to dst instead.
 __global__ void __launch_bounds__(kThreads) zero_update_kernel(const __grid_constant__ StepArgs a) {
+    allow_next_launch();
     if (a.ctrl->skip) {
         if (a.dst_master != a.src_master) copy_state(a);
-        return;
-    }
-    const float coef = a.ctrl->clip_coef;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
-         q += stride) {
-        const int64_t j = a.begin + q * kVec;
-        float p[kVec], m[kVec], v[kVec], g[kVec];
-        load8(a.src_master, j, p);
-        load8(a.src_m, j, m);
-        load8(a.src_v, j, v);
-        load8(a.gws, j, g);
+    } else {
+        const float coef = a.ctrl->clip_coef;
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+        for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+             q += stride) {
+            const int64_t j = a.begin + q * kVec;
+            float p[kVec], m[kVec], v[kVec], g[kVec];
+            load8(a.src_master, j, p);
+            load8(a.src_m, j, m);
+            load8(a.src_v, j, v);
+            load8(a.gws, j, g);
 #pragma unroll
-        for (int e = 0; e < kVec; ++e) {
-            const float gs = a.clip ? __fmul_rn(g[e], coef) : g[e];
-            adam_element(gs, p[e], m[e], v[e], a.s);
+            for (int e = 0; e < kVec; ++e) {
+                const float gs = a.clip ? __fmul_rn(g[e], coef) : g[e];
+                adam_element(gs, p[e], m[e], v[e], a.s);
+            }
+            store8(a.dst_master, j, p);
+            store8(a.dst_m, j, m);
+            store8(a.dst_v, j, v);
+            store_w8(a.dst_w, j, p);
         }
-        store8(a.dst_master, j, p);
-        store8(a.dst_m, j, m);
-        store8(a.dst_v, j, v);
-        store_w8(a.dst_w, j, p);
     }
+    // A sub-launch chained to the previous one completes only after it: the
+    // step's last launch completing then means the whole pass has.
+    if (threadIdx.x == 0) grid_dependency_wait();
 }
 
 // After a one-pass out-of-place step: a skipped step must leave dst equal to
@@ -507,6 +511,40 @@ bool launch(StepKernel fn, int device, const StepArgs& a, cudaStream_t stream,
     }
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError() == cudaSuccess;
+}
+
+// Largest range one launch covers.  A longer range (a large bucket, or the
+// whole vector when the step has one bucket) is split into near-equal
+// sub-launches chained by programmatic dependent launch: each one starts
+// streaming while the previous drains.  Measured on flat vectors of 1.2e8 to
+// 3e9 elements, a cap of 4M elements per launch was the most consistent
+// choice, against 6M to 16M.  For Psi = 1e9, N = 8 in 25M buckets it gave
+// 6.76 TB/s, against 6.54 TB/s with one launch per bucket.
+constexpr int64_t kLaunchElems = int64_t(1) << 22;
+constexpr int64_t kLaunchAlignGroups = 32;  // 256 elements
+
+// Launches fn over elements [begin, end) of a (a multiple of kVec long), in
+// sub-launches of at most kLaunchElems.  The first sub-launch overlaps the
+// kernel before it on the stream only if overlap_first; the others always
+// follow a sub-launch of the same range.
+bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t end,
+                  cudaStream_t stream, bool overlap_first) {
+    const int64_t groups = (end - begin) / kVec;
+    if (groups <= 0) return true;
+    const int64_t parts = (groups * kVec + kLaunchElems - 1) / kLaunchElems;
+    // Sub-launch sizes are a multiple of kLaunchAlignGroups, so each sub-launch
+    // starts as aligned as the range does.  With a range starting on a
+    // 512-byte boundary, every warp's 16-byte-per-lane access then covers
+    // whole 128-byte lines.  Split at an odd offset instead, each warp access
+    // straddles one more line: measured 8-9 % slower.
+    int64_t per = (groups + parts - 1) / parts;
+    per = (per + kLaunchAlignGroups - 1) / kLaunchAlignGroups * kLaunchAlignGroups;
+    for (int64_t k = 0, g0 = 0; g0 < groups; ++k, g0 += per) {
+        a.begin = begin + g0 * kVec;
+        a.n8 = (groups - g0 < per) ? groups - g0 : per;
+        if (!launch(fn, device, a, stream, k > 0 || overlap_first)) return false;
+    }
+    return true;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -716,8 +754,6 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     }
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
-    a.begin = begin;
-    a.n8 = (end - begin) / kVec;
     const bool bf16 = p->grad_dtype == ZERO_GRAD_BF16;
     const StepKernel fn = p->two_pass ? pick<ReduceK>(p->N, bf16) : pick<FusedK>(p->N, bf16);
     // Overlap with the previous bucket only when that launch is the one right
@@ -726,7 +762,8 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     // follows the wait for that slot's copy, so it is launched in plain
     // stream order.
     const bool overlap = p->overlap_buckets != 0 && begin > 0 && bucket_grads == nullptr;
-    if (!launch(fn, device, a, static_cast<cudaStream_t>(stream), overlap)) return ZERO_ERR_CUDA;
+    if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap))
+        return ZERO_ERR_CUDA;
     p->cursor = end;
     return ZERO_OK;
 }
@@ -754,11 +791,13 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
 
-    a.begin = 0;
-    a.n8 = p->psi_pad / kVec;
     if (p->two_pass) {
-        if (!launch(zero_update_kernel, device, a, stream)) return ZERO_ERR_CUDA;
+        // the first update launch waits for the finalize kernel in stream order
+        if (!launch_range(zero_update_kernel, device, a, 0, p->psi_pad, stream, false))
+            return ZERO_ERR_CUDA;
     } else if (!p->in_place && p->hp.skip_on_overflow) {
+        a.begin = 0;
+        a.n8 = p->psi_pad / kVec;
         if (!launch(zero_restore_kernel, device, a, stream)) return ZERO_ERR_CUDA;
     }
     p->state = 1;
