@@ -275,22 +275,24 @@ def run_ours(args, world, rank, local):
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
                    out_of_place=out_of_place, device=dev, master=master)
     buckets = opt.bucket_bounds()
-    # one event pair around each step's sequence of first-pass bucket launches
-    # (nothing is recorded between the launches, so they overlap as in zero_step)
-    span = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # One event pair per step around its sequence of first-pass launches.
+    # Nothing is recorded between the launches, so they overlap as in zero_step.
+    # When the host bookkeeping needs no step outcome (no skip, static loss
+    # scale) the host runs ahead of the device and the spans are read at the
+    # end.
     stream = torch.cuda.current_stream(dev)
+    spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(max(args.steps, args.warmup))]
 
-    def one_step(timed_spans: list | None):
-        ev = span if (args.api == "plan" and timed_spans is not None) else None
-        opt.enqueue(grads, stream, api=args.api, span_events=ev)
-        res = opt.finish(stream)
-        if not res["applied"]:
+    def one_step(k: int):
+        ev = spans[k] if args.api == "plan" else None
+        res = opt.step_async(grads, stream, api=args.api, span_events=ev)
+        if res is not None and not res["applied"]:
             raise RuntimeError("benchmark step was skipped: the synthetic gradients overflowed")
-        if ev is not None:
-            timed_spans.append(ev[0].elapsed_time(ev[1]))
 
-    for _ in range(args.warmup):
-        one_step(None)
+    for k in range(args.warmup):
+        one_step(k)
+    torch.cuda.synchronize(dev)
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -305,10 +307,14 @@ def run_ours(args, world, rank, local):
     launches0 = Z.zero_launch_count()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for _ in range(args.steps):
-        one_step(launch_ms)
+    for k in range(args.steps):
+        one_step(k)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    if not opt.last_result(stream)["applied"]:
+        raise RuntimeError("benchmark step was skipped: the synthetic gradients overflowed")
+    if args.api == "plan":
+        launch_ms = [a.elapsed_time(b) for a, b in spans[:args.steps]]
     group.barrier()
     launches = Z.zero_launch_count() - launches0
     clock_info = clocks.stop()
@@ -330,13 +336,15 @@ def run_ours(args, world, rank, local):
         b_kernel = wl.N * wl.grad_bytes if two_pass else b_alg
         achieved = b_kernel * wl.psi_pad / (per_step_kernel_ms / 1e3) / 1e9
         tpp = profiled_traffic_per_param()
+        n_launch = opt.first_pass_launches
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4),
-                    "traffic": (None if tpp is None else round(tpp * wl.psi_pad / len(buckets))),
+                    "traffic": (None if tpp is None else round(tpp * wl.psi_pad / n_launch)),
                     "peak_kind": peak_kind,
                     "kernel": "zero_reduce_kernel" if two_pass else "zero_fused_kernel",
-                    "launches_per_step": len(buckets),
-                    "avg_launch_ms": round(per_step_kernel_ms / len(buckets), 5),
+                    "buckets_per_step": len(buckets),
+                    "launches_per_step": n_launch,
+                    "avg_launch_ms": round(per_step_kernel_ms / n_launch, 5),
                     "alg_bytes_per_param": b_kernel}
     step_gbs = b_alg * wl.psi_pad / (ms / 1e3) / 1e9
 

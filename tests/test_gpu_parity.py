@@ -262,3 +262,29 @@ def test_plan_two_staging_slots(zero_lib, oracle_mod, dtype):
     got = {"master": st["master"].cpu().numpy(), "m": st["m"].cpu().numpy(),
            "v": st["v"].cpu().numpy(), "w": w.cpu().numpy().view(np.uint16)}
     compare_state(got, ref, exact=True)
+
+
+def test_async_steps_without_host_reads(zero_lib, oracle_mod):
+    """With no skip and a static loss scale, steps are enqueued back to back
+    without reading their outcome; the state after them matches the oracle."""
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    N, psi = 4, PSI_MULTI_SWEEP
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(3)) * 0.02
+    opt = ZeroAdam(psi_pad, N, "bf16", weight_decay=0.1, bucket_elems=1_000_000, device=dev,
+                   master=master.to(dev))
+    assert not opt.needs_result
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams(weight_decay=0.1)
+    all_grads = [_make_grads(N, psi, psi_pad, "bf16", 1e-3, 500 + s) for s in range(4)]
+    dev_grads = [[g.to(dev) for g in gs] for gs in all_grads]
+    for s, gs in enumerate(dev_grads):
+        assert opt.step_async(gs, api="plan" if s % 2 else "step") is None
+    assert opt.t == 4
+    for s, gs in enumerate(all_grads):
+        ores = oracle_mod.zero_step([_np(g) for g in gs], ref["master"], ref["m"], ref["v"],
+                                    ref["w"], hp, s + 1, 1.0, False)
+    compare_result(opt.last_result(), ores)
+    compare_state(state_to_numpy(opt.state()), ref, exact=True)

@@ -148,6 +148,7 @@ class ZeroAdam:
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if span_events is not None:
             span_events[0].record(s)
+        n0 = Z.zero_launch_count()
         for k, (b0, b1) in enumerate(self.bucket_bounds()):
             if bucket_events is not None:
                 bucket_events[k][0].record(s)
@@ -156,6 +157,8 @@ class ZeroAdam:
                 bucket_events[k][1].record(s)
         if span_events is not None:
             span_events[1].record(s)
+        # kernel launches of the first pass (the library splits long ranges)
+        self.first_pass_launches = Z.zero_launch_count() - n0
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
         if self.out_of_place:
             self.cur = 1 - self.cur
@@ -225,6 +228,35 @@ class ZeroAdam:
         self.last = {"applied": applied, "found_nonfinite": found, "grad_norm": norm,
                      "clip_coef": coef, "status": status}
         return self.last
+
+    @property
+    def needs_result(self) -> bool:
+        """Whether the host must read each step's outcome before the next one.
+        It must when a step can be skipped (t then does not advance) or the
+        loss scale reacts to overflow.  Otherwise every step applies and the
+        host can run ahead of the device."""
+        return bool(self.hp.skip_on_overflow) or self.scaler.dynamic
+
+    def step_async(self, grads, stream=None, api: str = "step", span_events=None) -> dict | None:
+        """Like step(), but without waiting when the outcome cannot change the
+        host's bookkeeping (see needs_result): t advances at once and None is
+        returned.  last_result() reads the latest outcome."""
+        self.enqueue(grads, stream, api, None, span_events)
+        if self.needs_result:
+            return self.finish(stream)
+        self.t += 1
+        return None
+
+    def last_result(self, stream=None) -> dict:
+        """Wait for the stream and read the most recent step's outcome, without
+        changing t or the loss scale."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        s.synchronize()
+        raw = self.result_t.clone()
+        Z.check(int(raw[0]), "zero_step (device)")
+        return {"applied": int(raw[0]) == Z.ZERO_OK, "found_nonfinite": bool(int(raw[1])),
+                "grad_norm": float(raw[2:3].view(torch.float32)[0]),
+                "clip_coef": float(raw[3:4].view(torch.float32)[0]), "status": int(raw[0])}
 
     def step(self, grads, stream=None, api: str = "step", bucket_events=None,
              span_events=None) -> dict:
