@@ -72,7 +72,11 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # ORACLE_LIB_OVERRIDE loads another build of the oracle's source;
+            # only the mutation test uses it, to check that the pins catch
+            # planted mistakes
+            override = os.environ.get("ORACLE_LIB_OVERRIDE")
+            lib = ctypes.CDLL(override if override else build())
             P = ctypes.c_void_p
             i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
             lib.orc_f32_to_bf16_array.argtypes = [P, P, i64]
