@@ -96,6 +96,9 @@ def _load():
             lib.orc_zero_step.restype = i32
             lib.orc_ddp_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
             lib.orc_ddp_step.restype = i32
+            lib.orc_zero_step_accum.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, i32, f64,
+                                                 i32, P]
+            lib.orc_zero_step_accum.restype = i32
             lib.orc_check_accumulate.argtypes = [P, i32, i32, i64, f32, P, P]
             lib.orc_step_window.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64,
                                             i32, i32, f32]
@@ -244,6 +247,23 @@ def zero_step(grads, master, m, v, w, hp: Hparams, t: int, loss_scale: float = 1
                                loss_scale, int(skip_on_overflow), ctypes.byref(res))
     if rc != 0:
         raise ValueError("oracle zero_step rejected its arguments")
+    return _result(res)
+
+
+def zero_step_accum(micro_grads, master, m, v, w, hp: Hparams, t: int, loss_scale: float = 1.0,
+                    skip_on_overflow: bool = False) -> dict:
+    """One step on the gradient accumulated over k micro-batches.
+    micro_grads[mb] is the list of N ranks' gradients of micro-batch mb."""
+    k = len(micro_grads)
+    N = len(micro_grads[0])
+    flat = [g for mb in micro_grads for g in mb]
+    res = _Result()
+    c = hp._c()
+    rc = _load().orc_zero_step_accum(_ptr_array(flat), _grad_dtype(flat), N, k, master.size,
+                                     _ptr(master), _ptr(m), _ptr(v), _ptr(w), ctypes.byref(c), t,
+                                     loss_scale, int(skip_on_overflow), ctypes.byref(res))
+    if rc != 0:
+        raise ValueError("oracle zero_step_accum rejected its arguments")
     return _result(res)
 
 

@@ -425,6 +425,66 @@ int orc_ddp_step(const void* const* grads, int32_t dtype, int32_t N, int64_t psi
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gradient accumulation over micro-batches (the DP-ZeRO blog, "stacking     */
+/* with other parallelism": under pipeline parallelism the gradient arrives  */
+/* micro-batch by micro-batch, so it is reduced and accumulated chunk by     */
+/* chunk instead of once at the end).                                        */
+/* Reading: the batch mean covers N * k contributions.  Each micro-batch adds  */
+/* its combined gradient, scaled by fp32(1/(N * k * loss_scale)), to the       */
+/* owner's FP32 accumulator in micro-batch order, starting from +0.  The      */
+/* step-wide checks and the update then use the accumulated gradient.         */
+/* ------------------------------------------------------------------------ */
+
+/* grads holds k * N pointers, micro-batch major: grads[mb * N + r]. */
+int orc_zero_step_accum(const void* const* grads, int32_t dtype, int32_t N, int32_t k,
+                        int64_t psi_pad, float* master, float* m, float* v, uint16_t* w,
+                        const orc_hparams* hp, int32_t t, double loss_scale,
+                        int32_t skip_on_overflow, orc_result* res)
+{
+    if (N < 1 || k < 1 || psi_pad < 0 || psi_pad % ((int64_t)N * ORC_PAD_UNIT) != 0)
+        return -1;
+    orc_scalars s;
+    orc_step_scalars(hp, t, N, loss_scale, &s);
+    float inv = (float)(1.0 / ((double)N * (double)k * loss_scale));
+    float* acc = (float*)malloc((size_t)(psi_pad > 0 ? psi_pad : 1) * sizeof(float));
+    if (!acc)
+        return -1;
+    for (int64_t j = 0; j < psi_pad; ++j)
+        acc[j] = 0.0f;
+    for (int32_t mb = 0; mb < k; ++mb)
+        for (int64_t j = 0; j < psi_pad; ++j)
+            acc[j] = acc[j] + orc_reduce_element(grads + (int64_t)mb * N, dtype, N, j, inv);
+    int32_t bad = 0;
+    double sumsq = 0.0;
+    for (int64_t j = 0; j < psi_pad; ++j) {
+        if (!orc_is_finite(acc[j]))
+            bad = 1;
+        sumsq = sumsq + (double)acc[j] * (double)acc[j];
+    }
+    res->found_nonfinite = bad;
+    res->sumsq = sumsq;
+    res->grad_norm = (float)sqrt(sumsq);
+    res->clip_coef = 1.0f;
+    if (skip_on_overflow && bad) {
+        res->applied = 0;
+        free(acc);
+        return 0;
+    }
+    if (hp->max_grad_norm > 0.0) {
+        res->clip_coef = orc_clip_coef(hp->max_grad_norm, sqrt(sumsq));
+        for (int64_t j = 0; j < psi_pad; ++j)
+            acc[j] = acc[j] * res->clip_coef;
+    }
+    for (int64_t j = 0; j < psi_pad; ++j) {
+        orc_adam_element(acc[j], &master[j], &m[j], &v[j], &s);
+        w[j] = orc_f32_to_bf16(master[j]);
+    }
+    res->applied = 1;
+    free(acc);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Windowed form, for vectors too large to hold on the host                   */
 /* The step is elementwise once the step-wide flag and norm are known, so a  */
 /* window of elements can be stepped on its own, exactly.                     */

@@ -51,11 +51,14 @@ MUTANTS = {
     "zero2_ledger_wrong": ("return weight_bytes * psi + (grad_bytes + optim_bytes) * sharded;",
                            "return (weight_bytes + grad_bytes) * psi + optim_bytes * sharded;"),
     "v_without_square": ("vv = s->b2 * vv + s->omb2 * (g * g);", "vv = s->b2 * vv + s->omb2 * g;"),
+    "accumulation_mean_without_k": (
+        "float inv = (float)(1.0 / ((double)N * (double)k * loss_scale));",
+        "float inv = (float)(1.0 / ((double)N * loss_scale));"),
 }
 
 PIN_TESTS = ["tests/test_oracle_adam.py", "tests/test_oracle_collectives.py",
              "tests/test_oracle_step.py", "tests/test_oracle_ledger.py",
-             "tests/test_oracle_bf16.py"]
+             "tests/test_oracle_bf16.py", "tests/test_oracle_accum.py"]
 
 
 def _build_mutant(name, tmp):
