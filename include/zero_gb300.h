@@ -105,7 +105,10 @@ typedef struct {
     double max_grad_norm;     /* > 0: clip by the global L2 norm; 0: no clipping   */
     int64_t step;             /* t >= 1: count of applied steps including this one */
     int32_t skip_on_overflow; /* 1: any non-finite combined gradient skips the step */
-    int32_t reserved;         /* must be 0                                         */
+    int32_t micro_batches;    /* k >= 2: the step's gradient is accumulated over k
+                                 micro-batches through the plan entry points (each
+                                 micro-batch's buckets reduce-scattered as they
+                                 arrive); 0 or 1: one batch                         */
     int64_t bucket_elems;     /* > 0: walk the flat vector in buckets of this many
                                  elements (a multiple of ZERO_BUCKET_ALIGN); 0: one
                                  bucket                                            */
@@ -144,8 +147,8 @@ int zero_shard_range(const zero_layout* layout, int32_t r, int64_t* begin, int64
  *   - per-CTA partial sums for the norm;
  *   - when the step must see the whole gradient before it may update
  *     anything, an FP32 copy of the combined gradient (psi_pad * 4 bytes).
- *     This is needed with clipping, and for an in-place step with
- *     skip_on_overflow.
+ *     This is needed with clipping, for an in-place step with
+ *     skip_on_overflow, and (as the accumulator) with micro_batches >= 2.
  * Returns 0 if the arguments are invalid. */
 size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, int32_t in_place);
 
@@ -246,15 +249,17 @@ typedef struct {
     int32_t in_place;
     int32_t two_pass;                  /* 1 if the update waits for a second pass          */
     int32_t state;                     /* 0 unset, 1 initialised, 2 begun                 */
+    int32_t micro_batch;               /* micro-batch the next bucket belongs to          */
     int32_t overlap_buckets;           /* 0 (as zero_plan_init leaves it): every bucket
                                           launch waits for all work before it on the
                                           stream.  1: the caller promises to enqueue
-                                          nothing on the stream between this plan's
+                                          nothing on the stream (no kernel, copy or
+                                          event wait) between this plan's
                                           zero_plan_bucket calls, so consecutive bucket
                                           launches may overlap (one starts while the
                                           previous drains), as zero_step runs them.
-                                          Buckets read through bucket_grads never
-                                          overlap.                                        */
+                                          The first bucket of each pass over the vector
+                                          never overlaps.                                 */
 } zero_plan;
 
 /* Fills *plan from the arguments of zero_step (dst == src) or zero_step_into
@@ -271,7 +276,18 @@ int zero_plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype
 /* Starts the step: clears the control block on `stream`. */
 int zero_plan_begin(zero_plan* plan, void* stream);
 
-/* First pass over elements [begin, end) of the flat vector.  begin must equal
+/* Gradient accumulation (hp->micro_batches = k >= 2; the DP-ZeRO blog,
+ * "stacking with other parallelism": under pipeline parallelism gradients
+ * arrive micro-batch by micro-batch, so they are reduced chunk by chunk as they
+ * go).  The plan then takes k passes of buckets over [0, psi_pad), one per
+ * micro-batch, each with that micro-batch's gradients.  Each bucket adds its
+ * combined gradient, scaled by fp32(1 / (N * k * loss_scale)), to the owner's
+ * FP32 accumulator in the workspace, in micro-batch order, from +0.  The
+ * overflow check, the norm, the clip and the update use the accumulated
+ * gradient.  zero_step and zero_step_into take one batch only and reject
+ * k >= 2.
+ *
+ * First pass over elements [begin, end) of the flat vector.  begin must equal
  * plan->cursor (buckets arrive in flat order, without gaps).  end is a multiple
  * of ZERO_BUCKET_ALIGN or psi_pad, and begin < end <= psi_pad.
  *   bucket_grads  NULL to read plan->grads[i] + begin; otherwise a host array of
@@ -285,7 +301,7 @@ int zero_plan_bucket(zero_plan* plan, int64_t begin, int64_t end,
                      const void* const* bucket_grads, void* stream);
 
 /* Ends the step once every element has been covered (plan->cursor ==
- * psi_pad).  It enqueues the step-wide decision and then the commit: the
+ * psi_pad), by every micro-batch when accumulating.  It enqueues the step-wide decision and then the commit: the
  * second pass, or the copy of a skipped out-of-place step.  result and the
  * return value are as for zero_step. */
 int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream);

@@ -124,7 +124,7 @@ def test_step_rejects_bad_sizes(zero_lib):
 @pytest.mark.parametrize("field,value", [("lr", -1.0), ("beta1", 1.0), ("beta2", -0.1),
                                          ("eps", 0.0), ("weight_decay", float("nan")),
                                          ("max_grad_norm", -1.0), ("step", 0),
-                                         ("skip_on_overflow", 2), ("reserved", 1),
+                                         ("skip_on_overflow", 2), ("micro_batches", -1),
                                          ("bucket_elems", 12)])
 def test_step_rejects_bad_hparams(zero_lib, field, value):
     Z = zero_lib
@@ -237,3 +237,27 @@ def test_plan_rejects_misuse(zero_lib):
                           12 * GB, 13 * GB, 128, 1, hp_skip, 1.0, 5 * GB,
                           Z.zero_workspace_bytes(128, hp_skip, False))
     assert rc == Z.ZERO_ERR_ARG
+
+
+def test_accumulation_rules(zero_lib):
+    Z = zero_lib
+    hp = Z.make_hparams(micro_batches=3)
+    n = 4 * 128 * 4
+    # accumulating needs the FP32 accumulator, in place or not
+    base = Z.zero_workspace_bytes(n, Z.make_hparams(), True)
+    assert Z.zero_workspace_bytes(n, hp, True) == base + 4 * n
+    assert Z.zero_workspace_bytes(n, hp, False) == base + 4 * n
+    # zero_step takes one batch only
+    assert _call(Z, hp=hp, ws_bytes=1 << 30) == Z.ZERO_ERR_ARG
+    # a plan for 3 micro-batches cannot end after covering the vector once
+    plan = Z.zero_plan()
+    rc = Z.zero_plan_init(plan, [6 * GB, 7 * GB, 8 * GB, 9 * GB], 0, 1 * GB, 2 * GB, 3 * GB, 4 * GB,
+                          1 * GB, 2 * GB, 3 * GB, 4 * GB, n, 4, hp, 1.0, 5 * GB,
+                          Z.zero_workspace_bytes(n, hp, True))
+    assert rc == Z.ZERO_OK and plan.two_pass == 1
+    plan.state = 2            # as if begun, without touching a device
+    plan.cursor = n
+    plan.micro_batch = 0
+    assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG
+    plan.micro_batch = 1
+    assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG

@@ -288,3 +288,44 @@ def test_async_steps_without_host_reads(zero_lib, oracle_mod):
                                     ref["w"], hp, s + 1, 1.0, False)
     compare_result(opt.last_result(), ores)
     compare_state(state_to_numpy(opt.state()), ref, exact=True)
+
+
+@pytest.mark.parametrize("N,k,dtype,clip,skip,out_of_place,bucket,wd", [
+    (4, 2, "bf16", 0.0, False, False, 0, 0.0),
+    (8, 3, "bf16", 0.0, True, True, 400_000, 0.0),
+    (3, 4, "fp32", 0.05, False, False, 262_144, 0.1),
+    (2, 2, "fp32", 0.0, True, False, 0, 0.1),
+    (4, 5, "bf16", 1.0, True, True, 1_000_000, 0.0),
+])
+def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, out_of_place,
+                               bucket, wd):
+    """k micro-batches reduce-scattered bucket by bucket into the owner's FP32
+    accumulator, then one update; against the oracle's accumulation.  With
+    the skip on, micro-batch 1 of step 2 carries a +inf."""
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    psi = PSI_MULTI_SWEEP if N >= 4 else PSI_SMALL
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(11)) * 0.02
+    opt = ZeroAdam(psi_pad, N, dtype, weight_decay=wd, max_grad_norm=clip, skip_on_overflow=skip,
+                   bucket_elems=bucket, loss_scale=256.0, out_of_place=out_of_place, device=dev,
+                   master=master.to(dev), micro_batches=k)
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams(weight_decay=wd, max_grad_norm=clip)
+    o_t = 0
+    for step in range(1, 4):
+        micro = [_make_grads(N, psi, psi_pad, dtype, 1e-3 * 256.0, 1000 * step + mb)
+                 for mb in range(k)]
+        if skip and step == 2:
+            micro[1][N - 1][777] = float("inf")
+        res = opt.step_accumulated([[g.to(dev) for g in mb] for mb in micro])
+        ores = oracle_mod.zero_step_accum([[_np(g) for g in mb] for mb in micro], ref["master"],
+                                          ref["m"], ref["v"], ref["w"], hp, o_t + 1, 256.0, skip)
+        compare_result(res, ores)
+        if ores["applied"]:
+            o_t += 1
+        assert opt.t == o_t
+        compare_state(state_to_numpy(opt.state()), ref, exact=clip == 0.0, tag=f"step {step} ")
+    if skip:
+        assert o_t == 2

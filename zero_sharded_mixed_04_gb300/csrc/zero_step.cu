@@ -94,6 +94,8 @@ struct StepArgs {
     int64_t gbase;       // flat index of grads[i][0] (the bucket start for a staging slot)
     int32_t N;
     int32_t clip;        // 1: multiply the gradient by ctrl->clip_coef before Adam
+    int32_t acc_first;   // accumulation: this is the first micro-batch (start from +0)
+    int32_t acc_last;    // accumulation: the last micro-batch (form the step-wide checks)
 };
 
 // ------------------------------------------------------------------ element math
@@ -332,6 +334,41 @@ __global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_cons
     finish_cta(a, bad, sumsq);
 }
 
+// One micro-batch of gradient accumulation: the reduce-scatter of this
+// micro-batch's contributions, scaled to the batch mean over all N * k of them,
+// added to the owner's FP32 accumulator in the workspace.  The last
+// micro-batch also forms the overflow flag and the norm of the accumulated
+// gradient.
+template <int NT, bool kBF16>
+__global__ void __launch_bounds__(kThreads) zero_accum_kernel(const __grid_constant__ StepArgs a) {
+    allow_next_launch();
+    unsigned bad = 0;
+    double sumsq = 0.0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+         q += stride) {
+        const int64_t j = a.begin + q * kVec;
+        float acc[kVec], g[kVec];
+        if (a.acc_first) {
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) acc[e] = 0.0f;
+        } else {
+            load8(a.gws, j, acc);
+        }
+        combine<NT, kBF16>(a, j, g);
+        float sq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            acc[e] = __fadd_rn(acc[e], __fmul_rn(g[e], a.s.inv));
+            bad |= is_nonfinite(acc[e]) ? 1u : 0u;
+            sq = fmaf(acc[e], acc[e], sq);
+        }
+        if (a.acc_last) sumsq += static_cast<double>(sq);
+        store8(a.gws, j, acc);
+    }
+    finish_cta(a, a.acc_last ? bad : 0u, sumsq);
+}
+
 __device__ __forceinline__ void copy_state(const StepArgs& a) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
@@ -436,6 +473,11 @@ struct FusedK {
 template <int NT, bool B>
 struct ReduceK {
     static constexpr StepKernel fn = zero_reduce_kernel<NT, B>;
+};
+
+template <int NT, bool B>
+struct AccumK {
+    static constexpr StepKernel fn = zero_accum_kernel<NT, B>;
 };
 
 template <template <int, bool> class K>
@@ -573,17 +615,25 @@ bool valid_hparams(const zero_adam_hparams* hp) {
            finite(hp->eps) && hp->eps > 0.0 && finite(hp->weight_decay) &&
            hp->weight_decay >= 0.0 && finite(hp->max_grad_norm) && hp->max_grad_norm >= 0.0 &&
            hp->step >= 1 && (hp->skip_on_overflow == 0 || hp->skip_on_overflow == 1) &&
-           hp->reserved == 0 && hp->bucket_elems >= 0 && hp->bucket_elems % ZERO_BUCKET_ALIGN == 0;
+           hp->micro_batches >= 0 && hp->bucket_elems >= 0 &&
+           hp->bucket_elems % ZERO_BUCKET_ALIGN == 0;
+}
+
+int32_t micro_batches_of(const zero_adam_hparams* hp) {
+    return hp->micro_batches > 1 ? hp->micro_batches : 1;
 }
 
 bool needs_two_passes(const zero_adam_hparams* hp, bool in_place) {
-    return hp->max_grad_norm > 0.0 || (in_place && hp->skip_on_overflow);
+    return hp->max_grad_norm > 0.0 || (in_place && hp->skip_on_overflow) ||
+           micro_batches_of(hp) > 1;
 }
 
 Scalars make_scalars(const zero_adam_hparams* hp, int32_t N, float loss_scale) {
     Scalars s;
     const double t = static_cast<double>(hp->step);
-    s.inv = static_cast<float>(1.0 / (static_cast<double>(N) * static_cast<double>(loss_scale)));
+    // the batch mean covers N ranks times the micro-batches accumulated
+    s.inv = static_cast<float>(1.0 / (static_cast<double>(N) * micro_batches_of(hp) *
+                                      static_cast<double>(loss_scale)));
     s.b1 = static_cast<float>(hp->beta1);
     s.omb1 = static_cast<float>(1.0 - hp->beta1);
     s.b2 = static_cast<float>(hp->beta2);
@@ -723,6 +773,7 @@ int plan_begin(zero_plan* p, void* stream) {
         cudaSuccess)
         return ZERO_ERR_CUDA;
     p->cursor = 0;
+    p->micro_batch = 0;
     p->state = 2;
     return ZERO_OK;
 }
@@ -755,21 +806,39 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
     const bool bf16 = p->grad_dtype == ZERO_GRAD_BF16;
-    const StepKernel fn = p->two_pass ? pick<ReduceK>(p->N, bf16) : pick<FusedK>(p->N, bf16);
+    const int32_t k = micro_batches_of(&p->hp);
+    StepKernel fn;
+    if (k > 1) {
+        fn = pick<AccumK>(p->N, bf16);
+        a.acc_first = p->micro_batch == 0 ? 1 : 0;
+        a.acc_last = p->micro_batch == k - 1 ? 1 : 0;
+    } else {
+        fn = p->two_pass ? pick<ReduceK>(p->N, bf16) : pick<FusedK>(p->N, bf16);
+    }
     // Overlap with the previous bucket only when that launch is the one right
     // before this on the stream.  The caller promises that by setting
-    // overlap_buckets; zero_step does.  A bucket read from a staging slot
-    // follows the wait for that slot's copy, so it is launched in plain
-    // stream order.
-    const bool overlap = p->overlap_buckets != 0 && begin > 0 && bucket_grads == nullptr;
+    // overlap_buckets (zero_step does).  A bucket read from a staging slot
+    // follows the wait for that slot's copy, so that caller leaves the flag at
+    // 0.  The first bucket of a pass (begin == 0) never overlaps: when
+    // accumulating it reads what the previous micro-batch wrote.
+    const bool overlap = p->overlap_buckets != 0 && begin > 0;
     if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap))
         return ZERO_ERR_CUDA;
     p->cursor = end;
+    // accumulating: a micro-batch that covered the vector hands over to the
+    // next, whose first bucket starts at 0 again.  That first bucket is never
+    // overlapped (begin == 0), because it reads what this micro-batch wrote.
+    if (p->cursor == p->psi_pad && p->micro_batch < k - 1) {
+        p->micro_batch += 1;
+        p->cursor = 0;
+    }
     return ZERO_OK;
 }
 
 int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
-    if (p == nullptr || p->state != 2 || p->cursor != p->psi_pad) return ZERO_ERR_ARG;
+    if (p == nullptr || p->state != 2 || p->cursor != p->psi_pad ||
+        p->micro_batch != micro_batches_of(&p->hp) - 1)
+        return ZERO_ERR_ARG;
     zero_step_result* result_dev = nullptr;
     if (result != nullptr) {
         cudaPointerAttributes attr;
@@ -819,6 +888,7 @@ int run_step(const void* const* grads, int32_t grad_dtype, const float* src_mast
              float* dst_m, float* dst_v, uint16_t* dst_w, int64_t psi_pad, int32_t N,
              const zero_adam_hparams* hp, float loss_scale, void* workspace,
              size_t workspace_bytes_given, zero_step_result* result, void* stream) {
+    if (hp != nullptr && micro_batches_of(hp) > 1) return ZERO_ERR_ARG;  // one batch only
     zero_plan plan;
     int rc = plan_init(&plan, grads, grad_dtype, src_master, src_m, src_v, src_w, dst_master, dst_m,
                        dst_v, dst_w, psi_pad, N, hp, loss_scale, workspace, workspace_bytes_given,

@@ -59,11 +59,11 @@ class ZeroAdam:
                  beta2=0.999, eps=1e-8, weight_decay=0.0, max_grad_norm=0.0,
                  skip_on_overflow=False, bucket_elems=0, loss_scale=1.0,
                  dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
-                 device="cuda", master: torch.Tensor | None = None):
+                 device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0):
         self.psi_pad, self.N = psi_pad, N
         self.grad_dtype = Z.ZERO_GRAD_BF16 if grad_dtype == "bf16" else Z.ZERO_GRAD_FP32
         self.hp = Z.make_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1,
-                                 skip_on_overflow, bucket_elems)
+                                 skip_on_overflow, bucket_elems, micro_batches)
         self.t = 0  # applied steps so far
         self.scaler = LossScaler(loss_scale, dynamic_loss_scale, growth_interval)
         self.out_of_place = out_of_place
@@ -163,6 +163,46 @@ class ZeroAdam:
         if self.out_of_place:
             self.cur = 1 - self.cur
         return rc
+
+    # ---------------------------------------------------------------- accumulation
+    def enqueue_accumulated(self, micro_grads, stream=None, span_events=None) -> int:
+        """Enqueue one step whose gradient is accumulated over the micro-batches
+        in ``micro_grads`` (a list of k lists of N gradient buffers; k must equal
+        the micro_batches this object was made with).  Each micro-batch's buckets
+        are reduce-scattered into the owner's FP32 accumulator in turn; the
+        update follows the last one."""
+        k = max(1, self.hp.micro_batches)
+        if len(micro_grads) != k:
+            raise ValueError(f"expected {k} micro-batches, got {len(micro_grads)}")
+        self.hp.step = self.t + 1
+        src = self._bufs[self.cur]
+        dst = self._bufs[1 - self.cur] if self.out_of_place else src
+        plan = Z.zero_plan()
+        Z.check(Z.zero_plan_init(plan, micro_grads[0], self.grad_dtype, src["master"], src["m"],
+                                 src["v"], src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
+                                 self.psi_pad, self.N, self.hp, self.scaler.scale,
+                                 self.workspace, self.ws_bytes), "zero_plan_init")
+        plan.overlap_buckets = 1
+        Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if span_events is not None:
+            span_events[0].record(s)
+        n0 = Z.zero_launch_count()
+        for grads in micro_grads:
+            for b0, b1 in self.bucket_bounds():
+                Z.check(Z.zero_plan_bucket(plan, b0, b1, [g[b0:b1] for g in grads], stream),
+                        "zero_plan_bucket")
+        if span_events is not None:
+            span_events[1].record(s)
+        self.first_pass_launches = Z.zero_launch_count() - n0
+        rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
+        if self.out_of_place:
+            self.cur = 1 - self.cur
+        return rc
+
+    def step_accumulated(self, micro_grads, stream=None) -> dict:
+        self.enqueue_accumulated(micro_grads, stream)
+        return self.finish(stream)
 
     # ---------------------------------------------------------------- host gradients
     def make_slots(self, bucket_elems: int | None = None) -> list[list[torch.Tensor]]:

@@ -56,7 +56,7 @@ class zero_adam_hparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double),
                 ("max_grad_norm", ctypes.c_double), ("step", ctypes.c_int64),
-                ("skip_on_overflow", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("skip_on_overflow", ctypes.c_int32), ("micro_batches", ctypes.c_int32),
                 ("bucket_elems", ctypes.c_int64)]
 
 
@@ -75,7 +75,8 @@ class zero_plan(ctypes.Structure):
                 ("cursor", ctypes.c_int64), ("hp", zero_adam_hparams),
                 ("loss_scale", ctypes.c_float), ("grad_dtype", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("in_place", ctypes.c_int32), ("two_pass", ctypes.c_int32),
-                ("state", ctypes.c_int32), ("overlap_buckets", ctypes.c_int32)]
+                ("state", ctypes.c_int32), ("micro_batch", ctypes.c_int32),
+                ("overlap_buckets", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -155,9 +156,9 @@ def _stream(s) -> int | None:
 
 def make_hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
                  max_grad_norm=0.0, step=1, skip_on_overflow=False,
-                 bucket_elems=0) -> zero_adam_hparams:
+                 bucket_elems=0, micro_batches=0) -> zero_adam_hparams:
     return zero_adam_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, step,
-                             int(bool(skip_on_overflow)), 0, bucket_elems)
+                             int(bool(skip_on_overflow)), micro_batches, bucket_elems)
 
 
 def zero_init_layout(tensor_numel, N: int):
