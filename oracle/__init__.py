@@ -99,6 +99,10 @@ def _load():
             lib.orc_zero_step_accum.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, i32, f64,
                                                  i32, P]
             lib.orc_zero_step_accum.restype = i32
+            lib.orc_gather_range.argtypes = [P, i32, i64, i64, i64, P]
+            lib.orc_gather_range.restype = i32
+            lib.orc_zero3_peak_bytes.argtypes = [P, i64, i32, i32, i32]
+            lib.orc_zero3_peak_bytes.restype = i64
             lib.orc_check_accumulate.argtypes = [P, i32, i32, i64, f32, P, P]
             lib.orc_step_window.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64,
                                             i32, i32, f32]
@@ -201,6 +205,24 @@ def loss_scale_update(scale: float, good_steps: int, found_nonfinite: bool,
     _load().orc_loss_scale_update(ctypes.byref(s), ctypes.byref(g), int(bool(found_nonfinite)),
                                   interval, backoff, growth)
     return s.value, g.value
+
+
+def gather_range(shards, begin: int, end: int) -> np.ndarray:
+    """Elements [begin, end) of the full view, from N BF16 shards (uint16)."""
+    shards = [np.ascontiguousarray(x, dtype=np.uint16) for x in shards]
+    out = np.empty(max(end - begin, 1), dtype=np.uint16)
+    rc = _load().orc_gather_range(_ptr_array(shards), len(shards), shards[0].size, begin, end,
+                                  _ptr(out))
+    if rc != 0:
+        raise ValueError("bad gather range")
+    return out[:end - begin]
+
+
+def zero3_peak_bytes(layer_numel, N: int, grad_bytes: int = 2, optim_bytes: int = 12) -> int:
+    """Peak bytes per rank under ZeRO-3 with the two-view gather schedule."""
+    arr = np.ascontiguousarray(layer_numel, dtype=np.int64)
+    return _load().orc_zero3_peak_bytes(_ptr(arr) if arr.size else None, arr.size, N, grad_bytes,
+                                        optim_bytes)
 
 
 # --------------------------------------------------------------------------- collectives

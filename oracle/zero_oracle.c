@@ -175,6 +175,54 @@ int64_t orc_comm_volume(int64_t psi, int32_t N, int32_t stage, int32_t ring_exac
 }
 
 /* ------------------------------------------------------------------------ */
+/* ZeRO-3: the working weights persist only as each rank's BF16 shard.  Before */
+/* a layer runs, its full view is all-gathered into temporary memory and     */
+/* released after use ([RC-T2 b2, N47]; [LEDGER "one full ZeRO-3              */
+/* computation"]).                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Elements [begin, end) of the full flat view, gathered from the N ranks'
+ * shards of `shard` elements each: element j lives in shard j / shard at
+ * offset j % shard. */
+int orc_gather_range(const uint16_t* const* shards, int32_t N, int64_t shard, int64_t begin,
+                     int64_t end, uint16_t* out)
+{
+    if (N < 1 || shard < 0 || begin < 0 || end < begin || end > (int64_t)N * shard)
+        return -1;
+    for (int64_t j = begin; j < end; ++j)
+        out[j - begin] = shards[j / shard][j % shard];
+    return 0;
+}
+
+/* Peak bytes one rank holds under ZeRO-3 when the layers (in run order,
+ * layer_numel[i] elements each) are gathered one ahead into two temporary
+ * BF16 views -- one in use, one being prefetched ([DPZERO "offloading the
+ * shard to the CPU: two buffers"]) -- and each view is released after its
+ * layer ran: the persistent ZeRO-3 subtotal plus the largest pair of
+ * neighbouring layers alive together.  The pages stress that the persistent
+ * subtotal is not the peak ([RC-T2 b2, N47]); activations and communication
+ * buffers are left out, as in the ledger. */
+int64_t orc_zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers, int32_t N,
+                             int32_t grad_bytes, int32_t optim_bytes)
+{
+    if (n_layers < 0 || N < 1)
+        return -1;
+    int64_t psi = 0, live = 0;
+    for (int64_t i = 0; i < n_layers; ++i) {
+        if (layer_numel[i] < 0)
+            return -1;
+        psi += layer_numel[i];
+        int64_t pair = layer_numel[i] + (i + 1 < n_layers ? layer_numel[i + 1] : 0);
+        if (pair > live)
+            live = pair;
+    }
+    int64_t persistent = orc_ledger_bytes(psi, N, 3, grad_bytes, optim_bytes);
+    if (persistent < 0)
+        return -1;
+    return persistent + 2 * live;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step-wide scalars                                                          */
 /* ------------------------------------------------------------------------ */
 

@@ -51,6 +51,11 @@ MUTANTS = {
     "zero2_ledger_wrong": ("return weight_bytes * psi + (grad_bytes + optim_bytes) * sharded;",
                            "return (weight_bytes + grad_bytes) * psi + optim_bytes * sharded;"),
     "v_without_square": ("vv = s->b2 * vv + s->omb2 * (g * g);", "vv = s->b2 * vv + s->omb2 * g;"),
+    "gather_shard_index_transposed": ("out[j - begin] = shards[j / shard][j % shard];",
+                                      "out[j - begin] = shards[j % N][j / N];"),
+    "peak_forgets_prefetched_view": (
+        "int64_t pair = layer_numel[i] + (i + 1 < n_layers ? layer_numel[i + 1] : 0);",
+        "int64_t pair = layer_numel[i];"),
     "accumulation_mean_without_k": (
         "float inv = (float)(1.0 / ((double)N * (double)k * loss_scale));",
         "float inv = (float)(1.0 / ((double)N * loss_scale));"),
@@ -58,7 +63,8 @@ MUTANTS = {
 
 PIN_TESTS = ["tests/test_oracle_adam.py", "tests/test_oracle_collectives.py",
              "tests/test_oracle_step.py", "tests/test_oracle_ledger.py",
-             "tests/test_oracle_bf16.py", "tests/test_oracle_accum.py"]
+             "tests/test_oracle_bf16.py", "tests/test_oracle_accum.py",
+             "tests/test_oracle_zero3.py"]
 
 
 def _build_mutant(name, tmp):
