@@ -70,6 +70,11 @@ def parse_args(argv=None):
     ap.add_argument("--micro-batches", type=int, default=0,
                     help="accumulate each step's gradient over this many micro-batches "
                          "(reduce-scattered bucket by bucket); 0 = one batch")
+    ap.add_argument("--zero3-gather", action="store_true",
+                    help="time the ZeRO-3 per-layer gather (two views, one-ahead prefetch) "
+                         "over the workload's layers instead of the step")
+    ap.add_argument("--zero3-layer-elems", type=int, default=50_000_000,
+                    help="layer size for flat workloads in --zero3-gather")
     ap.add_argument("--psi", type=int, default=0,
                     help="reduced parameter count of the same workload (profiling captures "
                          "only; the benchmark line is the full size)")
@@ -516,9 +521,77 @@ def run_reference(args, world, rank):
     }), flush=True)
 
 
+def zero3_layers(wl, layout_offsets, sizes, layer_elems):
+    """Flat [begin, end) ranges of the workload's layers: GPT-2-small's
+    embedding, twelve blocks and final norm; equal layers for flat vectors."""
+    if wl.name.startswith("gpt2small"):
+        bounds = [0, 1] + [1 + 10 * (i + 1) for i in range(12)] + [len(sizes)]
+        return [(layout_offsets[bounds[i]],
+                 layout_offsets[bounds[i + 1] - 1] + sizes[bounds[i + 1] - 1])
+                for i in range(len(bounds) - 1)]
+    return [(b, min(wl.psi, b + layer_elems)) for b in range(0, wl.psi, layer_elems)]
+
+
+def run_zero3_gather(args, world, rank, local):
+    """Times passes of the ZeRO-3 per-layer gather over the workload's layers,
+    after one step has written the owners' BF16 shards."""
+    import torch
+    from zero_sharded_mixed_04_gb300 import build
+    build.build_library()
+    from zero_sharded_mixed_04_gb300 import synth
+    from zero_sharded_mixed_04_gb300 import zero as Z
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam, Zero3Views
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = select_workload(args)
+    sizes = wl.sizes
+    rc, lay, offs = Z.zero_init_layout(sizes, wl.N)
+    Z.check(rc, "zero_init_layout")
+    layers = zero3_layers(wl, offs, sizes, args.zero3_layer_elems)
+    grads = synth.make_grads(wl, 1, dev)
+    opt = ZeroAdam(wl.psi_pad, wl.N, wl.grad_dtype, lr=wl.lr, weight_decay=wl.weight_decay,
+                   loss_scale=wl.loss_scale, device=dev, master=synth.make_master(wl, dev))
+    opt.step(grads)
+    del grads
+    torch.cuda.empty_cache()
+    w = opt.state()["w"]
+    S = lay.shard
+    views = Zero3Views([w[r * S:(r + 1) * S] for r in range(wl.N)], S, layers, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        views.run(lambda i, v: None)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        views.run(lambda i, v: None)   # the stream waits for every layer's gather
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = read_peaks()
+    gbs = 4 * wl.psi / (ms / 1e3) / 1e9   # 2 B read from a shard + 2 B written to a view
+    numel = [e - b for b, e in layers]
+    if rank == 0:
+        print(json.dumps({
+            "metric": "ZeRO-3 per-layer gather: gathered params/s (two views, one-ahead prefetch)",
+            "value": round(wl.psi / (ms / 1e3), 1), "unit": "params/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_pass": round(ms, 4),
+            "higher_is_better": True,
+            "config": {"workload": wl.name, "N": wl.N, "layers": len(layers),
+                       "largest_layer": max(numel)},
+            "achieved_gbs": round(gbs, 1), "peak": peak, "peak_kind": peak_kind,
+            "frac": round(gbs / peak, 4),
+            "ledger_bytes_per_rank": {"zero3_persistent": Z.zero_ledger(wl.psi, wl.N, 3),
+                                      "zero3_peak_two_views": Z.zero3_peak_bytes(numel, wl.N)},
+        }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
+    if args.zero3_gather and args.impl == "ours":
+        run_zero3_gather(args, world, rank, local)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

@@ -306,6 +306,44 @@ int zero_plan_bucket(zero_plan* plan, int64_t begin, int64_t end,
  * return value are as for zero_step. */
 int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream);
 
+/* ------------------------------------------------------------------------
+ * ZeRO-3: per-layer gather of the working weights.
+ *
+ * Under ZeRO-3 each rank keeps only its 1/N shard of the BF16 working weights.
+ * Before a layer runs, its full view is all-gathered into temporary memory and
+ * released once the layer has run (RC-T2 slide b2 and note N47; ledger page,
+ * "one full ZeRO-3 computation").  Here the N shards are the owners' slices
+ * of the flat vector.  A step's all-gather writes them: shard r is
+ * w_bf16 + r*S.  They may equally be N separate buffers.
+ * ------------------------------------------------------------------------ */
+
+/* Copies elements [begin, end) of the full flat view into `view`.  Element j
+ * is read from shards[j / shard] at offset j % shard.
+ *   shards   host array of N device pointers, each ZERO_ALIGN_BYTES-aligned,
+ *            holding `shard` BF16 values
+ *   shard    elements per shard, a multiple of ZERO_BUCKET_ALIGN (every
+ *            layout from zero_init_layout qualifies)
+ *   view     device buffer of end - begin BF16 values, ZERO_ALIGN_BYTES-aligned;
+ *            it must not overlap a shard
+ * Any 0 <= begin <= end <= N * shard is accepted.  A begin that is a multiple
+ * of ZERO_BUCKET_ALIGN takes a 16-byte vector path; any other begin takes an
+ * element-by-element path.  Enqueued on `stream`.  Returns ZERO_OK, or
+ * ZERO_ERR_ARG / ZERO_ERR_ALIGN / ZERO_ERR_OVERLAP / ZERO_ERR_CUDA before
+ * anything is enqueued. */
+int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t shard, int64_t begin,
+                 int64_t end, uint16_t* view, void* stream);
+
+/* Peak bytes one rank holds under ZeRO-3 when the layers, of layer_numel[i]
+ * elements in run order, are gathered one ahead into two BF16 views (one in
+ * use, one being prefetched) and each view is released after its layer ran.
+ * That is the persistent ZeRO-3 subtotal (zero_ledger(psi, N, 3, ...)) plus 2 B
+ * times the largest sum of two neighbouring layers.  The pages stress that the
+ * persistent subtotal (32 GB for 8e9 parameters on 4 ranks) is not the peak.
+ * Activations and communication buffers are left out, as in the ledger.
+ * Host only.  Returns -1 on a bad argument. */
+int64_t zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers, int32_t N,
+                         int32_t grad_bytes, int32_t optim_bytes);
+
 /* Persistent bytes one rank holds under a ZeRO stage: 0 = replicated data
  * parallelism, 1 = optimizer state sharded, 2 = also gradients, 3 = also the
  * working weights.  A replicated part counts psi elements.  A sharded part

@@ -19,7 +19,7 @@ def _declared_functions():
             continue
         text = open(os.path.join(ROOT, "include", fn)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(zero_\w+)\s*\(", text, flags=re.M)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(zero3?_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
@@ -261,3 +261,24 @@ def test_accumulation_rules(zero_lib):
     assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG
     plan.micro_batch = 1
     assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG
+
+
+@pytest.mark.parametrize("layers", [[5, 9, 3, 9], [100], [], [1000, 1, 1, 999], [38_597_376, 7_082_496]])
+@pytest.mark.parametrize("N", [1, 4, 8])
+def test_zero3_peak_matches_oracle(zero_lib, oracle_mod, layers, N):
+    assert zero_lib.zero3_peak_bytes(layers, N) == oracle_mod.zero3_peak_bytes(layers, N)
+    assert zero_lib.zero3_peak_bytes(layers, N, 4, 12) == oracle_mod.zero3_peak_bytes(layers, N, 4, 12)
+
+
+def test_zero3_gather_rejects_bad_arguments(zero_lib):
+    Z = zero_lib
+    shards = [1 * GB, 2 * GB, 3 * GB, 4 * GB]
+    assert Z.zero3_gather(shards, 4, 1024, 0, 4097, 5 * GB, 0) == Z.ZERO_ERR_ARG   # past the end
+    assert Z.zero3_gather(shards, 4, 1020, 0, 16, 5 * GB, 0) == Z.ZERO_ERR_ARG     # shard % 8
+    assert Z.zero3_gather(shards, 4, 1024, 10, 5, 5 * GB, 0) == Z.ZERO_ERR_ARG     # end < begin
+    assert Z.zero3_gather(shards, 0, 1024, 0, 0, 5 * GB, 0) == Z.ZERO_ERR_ARG
+    assert Z.zero3_gather(shards, 4, 1024, 0, 16, 5 * GB + 2, 0) == Z.ZERO_ERR_ALIGN
+    assert Z.zero3_gather([1 * GB + 8, 2 * GB, 3 * GB, 4 * GB], 4, 1024, 0, 16, 5 * GB, 0) == \
+        Z.ZERO_ERR_ALIGN
+    assert Z.zero3_gather(shards, 4, 1024, 0, 16, 2 * GB + 64, 0) == Z.ZERO_ERR_OVERLAP
+    assert Z.zero3_gather(shards, 4, 1024, 7, 7, None, 0) == Z.ZERO_OK              # empty: nothing

@@ -74,6 +74,22 @@ extern "C" int64_t zero_ledger(int64_t psi, int32_t N, int32_t stage, int32_t gr
     }
 }
 
+extern "C" int64_t zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers, int32_t N,
+                                   int32_t grad_bytes, int32_t optim_bytes) {
+    if (n_layers < 0 || N < 1 || (n_layers > 0 && layer_numel == nullptr)) return -1;
+    int64_t psi = 0;
+    int64_t live = 0;  // the most elements alive in the two views at once
+    for (int64_t i = 0; i < n_layers; ++i) {
+        if (layer_numel[i] < 0) return -1;
+        psi += layer_numel[i];
+        const int64_t next = (i + 1 < n_layers) ? layer_numel[i + 1] : 0;
+        if (layer_numel[i] + next > live) live = layer_numel[i] + next;
+    }
+    const int64_t persistent = zero_ledger(psi, N, 3, grad_bytes, optim_bytes);
+    if (persistent < 0) return -1;
+    return persistent + 2 * live;  // BF16 views
+}
+
 extern "C" int64_t zero_comm_volume(int64_t psi, int32_t N, int32_t stage) {
     if (psi < 0 || N < 1 || stage < 0 || stage > 3) return -1;
     // reduce-scatter + all-gather (= one all-reduce); ZeRO-3 gathers the

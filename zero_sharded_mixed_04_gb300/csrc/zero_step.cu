@@ -961,6 +961,124 @@ extern "C" int zero_plan_end(zero_plan* plan, zero_step_result* result, void* st
 
 extern "C" uint64_t zero_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+// ------------------------------------------------------------------ ZeRO-3 layer gather
+//
+// The full view of a layer, assembled from the owners' BF16 shards: the
+// all-gather before a layer runs under ZeRO-3.  Pure data movement: 2 B read
+// and 2 B written per element.
+
+namespace {
+
+struct GatherArgs {
+    const uint16_t* shards[ZERO_MAX_RANKS];
+    uint16_t* view;
+    int64_t shard;  // elements per shard (a multiple of kVec)
+    int64_t begin;  // first element of the range in the full view
+    int64_t n;      // elements in the range
+    // The range cut at shard boundaries (vector path): segment s copies
+    // seg_len[s] elements from shard seg_shard[s] at seg_src[s] to the view at
+    // seg_dst[s].  At most one segment per shard.
+    int64_t seg_src[ZERO_MAX_RANKS];
+    int64_t seg_dst[ZERO_MAX_RANKS];
+    int64_t seg_len[ZERO_MAX_RANKS];
+    int32_t seg_shard[ZERO_MAX_RANKS];
+    int32_t segments;
+};
+
+constexpr int kGatherUnroll = 4;  // 16-byte vectors in flight per thread
+
+// begin is a multiple of kVec, so every segment is a whole number of 8-element
+// groups on both sides; the last segment may end with n % 8 single elements.
+__global__ void __launch_bounds__(kThreads) zero3_gather_vec_kernel(const __grid_constant__ GatherArgs g) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (int s = 0; s < g.segments; ++s) {
+        const uint4* src = reinterpret_cast<const uint4*>(g.shards[g.seg_shard[s]] + g.seg_src[s]);
+        uint4* dst = reinterpret_cast<uint4*>(g.view + g.seg_dst[s]);
+        const int64_t n8 = g.seg_len[s] / kVec;
+        int64_t q = tid;
+        for (; q + (kGatherUnroll - 1) * stride < n8; q += kGatherUnroll * stride) {
+            uint4 x[kGatherUnroll];
+#pragma unroll
+            for (int u = 0; u < kGatherUnroll; ++u) x[u] = __ldcs(src + q + u * stride);
+#pragma unroll
+            for (int u = 0; u < kGatherUnroll; ++u) __stcs(dst + q + u * stride, x[u]);
+        }
+        for (; q < n8; q += stride) __stcs(dst + q, __ldcs(src + q));
+        const int64_t tail = g.seg_len[s] - n8 * kVec;  // only the last segment has one
+        if (tid < tail) {
+            const int64_t i = n8 * kVec + tid;
+            g.view[g.seg_dst[s] + i] = g.shards[g.seg_shard[s]][g.seg_src[s] + i];
+        }
+    }
+}
+
+// Any begin: element by element (a layer that starts at an odd offset).
+__global__ void __launch_bounds__(kThreads) zero3_gather_elem_kernel(const __grid_constant__ GatherArgs g) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < g.n; i += stride) {
+        const int64_t j = g.begin + i;
+        const int64_t r = j / g.shard;
+        g.view[i] = g.shards[r][j - r * g.shard];
+    }
+}
+
+}  // namespace
+
+extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t shard, int64_t begin,
+                            int64_t end, uint16_t* view, void* stream) {
+    if (shards == nullptr || N < 1 || N > ZERO_MAX_RANKS || shard < 0 || shard % kVec != 0 ||
+        begin < 0 || end < begin || end > static_cast<int64_t>(N) * shard)
+        return ZERO_ERR_ARG;
+    const int64_t n = end - begin;
+    if (n == 0) return ZERO_OK;
+    if (view == nullptr) return ZERO_ERR_ARG;
+    if (!aligned(view, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+    GatherArgs g{};
+    const uintptr_t vlo = reinterpret_cast<uintptr_t>(view), vhi = vlo + 2 * static_cast<uintptr_t>(n);
+    for (int i = 0; i < N; ++i) {
+        if (shards[i] == nullptr) return ZERO_ERR_ARG;
+        if (!aligned(shards[i], ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(shards[i]);
+        const uintptr_t hi = lo + 2 * static_cast<uintptr_t>(shard);
+        if (lo < vhi && vlo < hi) return ZERO_ERR_OVERLAP;
+        g.shards[i] = shards[i];
+    }
+    g.view = view;
+    g.shard = shard;
+    g.begin = begin;
+    g.n = n;
+    // cut [begin, end) at shard boundaries
+    g.segments = 0;
+    for (int64_t at = begin; at < end;) {
+        const int64_t r = at / shard;
+        const int64_t stop = (end < (r + 1) * shard) ? end : (r + 1) * shard;
+        g.seg_shard[g.segments] = static_cast<int32_t>(r);
+        g.seg_src[g.segments] = at - r * shard;
+        g.seg_dst[g.segments] = at - begin;
+        g.seg_len[g.segments] = stop - at;
+        ++g.segments;
+        at = stop;
+    }
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
+    const bool vec = begin % kVec == 0;
+    const void* fn = vec ? reinterpret_cast<const void*>(zero3_gather_vec_kernel)
+                         : reinterpret_cast<const void*>(zero3_gather_elem_kernel);
+    const int64_t units = vec ? (n + kVec * kGatherUnroll - 1) / (kVec * kGatherUnroll) : n;
+    const int64_t full = static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, kThreads);
+    int64_t grid = (units + kThreads - 1) / kThreads;
+    if (grid > full) grid = full;
+    if (grid < 1) grid = 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (vec)
+        zero3_gather_vec_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(g);
+    else
+        zero3_gather_elem_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(g);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ no-allocation entry point
 //
 // For callers that cannot allocate device memory: zero_step with its

@@ -302,3 +302,49 @@ class ZeroAdam:
              span_events=None) -> dict:
         self.enqueue(grads, stream, api, bucket_events, span_events)
         return self.finish(stream)
+
+
+class Zero3Views:
+    """ZeRO-3 per-layer gather with two views: before layer i runs, layer i + 1
+    is gathered into the other view on a side stream; a view is reused only
+    after the layer that held it ran (released).  The layers are flat ranges
+    [begin, end) of the vector whose BF16 shards are ``shards`` (N device
+    buffers of ``shard`` elements, e.g. the owners' slices of a step's
+    working weights)."""
+
+    def __init__(self, shards, shard: int, layers, device="cuda"):
+        self.shards = list(shards)
+        self.N = len(self.shards)
+        self.shard = shard
+        self.layers = [(int(b), int(e)) for b, e in layers]
+        self.device = torch.device(device)
+        most = max((e - b for b, e in self.layers), default=0)
+        self.views = [torch.empty(max(most, 1), dtype=torch.int16, device=self.device)
+                      for _ in range(2)]
+        self.side = torch.cuda.Stream(self.device)
+        self.gathered = [torch.cuda.Event(), torch.cuda.Event()]
+        self.released = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def _gather(self, i: int) -> None:
+        b, e = self.layers[i]
+        slot = i % 2
+        self.side.wait_event(self.released[slot])  # no-op before the first record
+        Z.check(Z.zero3_gather(self.shards, self.N, self.shard, b, e, self.views[slot],
+                               self.side), "zero3_gather")
+        self.gathered[slot].record(self.side)
+
+    def run(self, use, stream=None) -> None:
+        """Calls use(i, view) for every layer in order, on ``stream``, where view
+        is the layer's gathered BF16 values (int16 bits)."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if not self.layers:
+            return
+        self.side.wait_stream(s)  # the shards are ready on s
+        self._gather(0)
+        for i, (b, e) in enumerate(self.layers):
+            if i + 1 < len(self.layers):
+                self._gather(i + 1)           # prefetch into the other view
+            slot = i % 2
+            s.wait_event(self.gathered[slot])
+            use(i, self.views[slot][:e - b])
+            self.released[slot].record(s)     # the view may be refilled

@@ -109,6 +109,10 @@ _lib.zero_plan_end.restype = ctypes.c_int
 _lib.zero_step_noalloc.argtypes = [_P, _i32, _P, _P, _P, _P, _i64, _i32,
                                    ctypes.POINTER(zero_adam_hparams), _f32, _P, _P]
 _lib.zero_step_noalloc.restype = ctypes.c_int
+_lib.zero3_gather.argtypes = [_P, _i32, _i64, _i64, _i64, _P, _P]
+_lib.zero3_gather.restype = ctypes.c_int
+_lib.zero3_peak_bytes.argtypes = [_P, _i64, _i32, _i32, _i32]
+_lib.zero3_peak_bytes.restype = _i64
 _lib.zero_ledger.argtypes = [_i64, _i32, _i32, _i32, _i32]
 _lib.zero_ledger.restype = _i64
 _lib.zero_comm_volume.argtypes = [_i64, _i32, _i32]
@@ -240,6 +244,18 @@ def zero_step_noalloc(grads, grad_dtype: int, master, m, v, w_bf16, psi_pad: int
                                   loss_scale, _addr(result), _stream(stream))
 
 
+def zero3_gather(shards, N: int, shard: int, begin: int, end: int, view, stream=None) -> int:
+    """Elements [begin, end) of the full BF16 view, gathered from N shards."""
+    arr = (ctypes.c_void_p * max(len(shards), 1))(*[_addr(x) for x in shards])
+    return _lib.zero3_gather(arr, N, shard, begin, end, _addr(view), _stream(stream))
+
+
+def zero3_peak_bytes(layer_numel, N: int, grad_bytes: int = 2, optim_bytes: int = 12) -> int:
+    n = len(layer_numel)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in layer_numel])
+    return _lib.zero3_peak_bytes(arr if n else None, n, N, grad_bytes, optim_bytes)
+
+
 def zero_ledger(psi: int, N: int, stage: int, grad_bytes: int = 2, optim_bytes: int = 12) -> int:
     return _lib.zero_ledger(psi, N, stage, grad_bytes, optim_bytes)
 
@@ -261,4 +277,4 @@ def exported_symbols() -> list[str]:
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
             "zero_step_into", "zero_plan_init", "zero_plan_begin", "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
-            "zero_launch_count", "zero_step_noalloc"]
+            "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes"]
