@@ -67,6 +67,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 10)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-grad-accum", action="store_true",
+                    help="keep the owner's FP32 gradient shard in pinned host memory "
+                         "(reached over the host link); forces the two-pass form")
     ap.add_argument("--micro-batches", type=int, default=0,
                     help="accumulate each step's gradient over this many micro-batches "
                          "(reduce-scattered bucket by bucket); 0 = one batch")
@@ -282,7 +285,7 @@ def run_ours(args, world, rank, local):
                    skip_on_overflow=wl.skip_on_overflow, bucket_elems=wl.bucket_elems,
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
                    out_of_place=out_of_place, device=dev, master=master,
-                   micro_batches=args.micro_batches)
+                   micro_batches=args.micro_batches, host_grad_accum=args.host_grad_accum)
     buckets = opt.bucket_bounds()
     k_micro = max(1, args.micro_batches)
     # One event pair per step around its sequence of first-pass launches.
@@ -341,7 +344,8 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = read_peaks()
     b_alg = alg_bytes_per_param(wl)
     roofline = None
-    two_pass = opt.hp.max_grad_norm > 0 or (not out_of_place and opt.hp.skip_on_overflow)
+    two_pass = (opt.hp.max_grad_norm > 0 or (not out_of_place and opt.hp.skip_on_overflow)
+                or args.host_grad_accum)
     if launch_ms:
         # the bucket launches of a step: their total span over the launch count
         # is the average launch duration
@@ -395,6 +399,7 @@ def run_ours(args, world, rank, local):
                    "loss_scale": wl.loss_scale, "dynamic_loss_scale": wl.dynamic_loss_scale,
                    "skip_on_overflow": wl.skip_on_overflow, "max_grad_norm": wl.max_grad_norm,
                    "micro_batches": k_micro,
+                   "grad_shard": "pinned host memory" if args.host_grad_accum else "HBM",
                    "entry": ("zero_plan_* (= zero_step_into)" if args.api == "plan"
                              else "zero_step_into") if out_of_place else
                    ("zero_plan_* (= zero_step)" if args.api == "plan" else "zero_step"),

@@ -240,6 +240,9 @@ typedef struct {
     uint16_t* dst_w_bf16;
     void* workspace;
     size_t workspace_bytes;
+    float* grad_accum;                 /* the FP32 combined-gradient buffer of the two-pass
+                                          form: NULL = inside the workspace; otherwise the
+                                          caller's buffer (see zero_plan_init_ex)          */
     int64_t psi_pad;
     int64_t cursor;                    /* next element a bucket must start at             */
     zero_adam_hparams hp;
@@ -272,6 +275,29 @@ int zero_plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype
                    uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
                    const zero_adam_hparams* hp, float loss_scale, void* workspace,
                    size_t workspace_bytes);
+
+/* Bytes of the workspace's control part: what the workspace needs when the
+ * combined gradient is kept in a caller buffer (zero_plan_init_ex). */
+#define ZERO_WORKSPACE_CONTROL_BYTES 16640
+
+/* zero_plan_init with the owner's FP32 combined gradient (the reduced
+ * gradient shard, or the accumulator with micro_batches >= 2) kept in
+ * grad_accum.  That is a caller buffer of psi_pad floats, 16-byte aligned and
+ * addressable by the device: device memory, or pinned host memory.  With
+ * pinned host memory the gradient shard leaves the GPU altogether (DP-ZeRO
+ * blog, "offloading the shard to the CPU: two buffers are enough").  The GPU
+ * keeps only the buckets in flight, for instance in two staging slots, and
+ * the kernels add each reduced bucket into the host shard over NVLink-C2C.
+ * A non-NULL grad_accum forces the two-pass form, since the update reads the
+ * gradient from there.  The workspace then needs only
+ * ZERO_WORKSPACE_CONTROL_BYTES.  NULL behaves as zero_plan_init.  grad_accum
+ * must not overlap any other buffer of the step. */
+int zero_plan_init_ex(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
+                      const float* src_master, const float* src_m, const float* src_v,
+                      const uint16_t* src_w_bf16, float* dst_master, float* dst_m, float* dst_v,
+                      uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
+                      const zero_adam_hparams* hp, float loss_scale, void* workspace,
+                      size_t workspace_bytes, float* grad_accum);
 
 /* Starts the step: clears the control block on `stream`. */
 int zero_plan_begin(zero_plan* plan, void* stream);

@@ -48,7 +48,7 @@ def _np(t):
 def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, wd=0.0,
                clip=0.0, skip=False, out_of_place=False, bucket=0, loss_scale=1.0,
                dynamic=False, growth_interval=2000, sigma=1e-3, bad_step=0, bad_value=np.inf,
-               seed=1234, api="step", per_bucket_events=False):
+               seed=1234, api="step", per_bucket_events=False, host_accum=False):
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     unit = N * 128
@@ -60,7 +60,8 @@ def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, 
     opt = ZeroAdam(psi_pad, N, dtype, lr=lr, weight_decay=wd, max_grad_norm=clip,
                    skip_on_overflow=skip, bucket_elems=bucket, loss_scale=loss_scale,
                    dynamic_loss_scale=dynamic, growth_interval=growth_interval,
-                   out_of_place=out_of_place, device=dev, master=master.to(dev))
+                   out_of_place=out_of_place, device=dev, master=master.to(dev),
+                   host_grad_accum=host_accum)
     ref = _oracle_state(master.numpy())
     hp = oracle_mod.Hparams(lr=lr, weight_decay=wd, max_grad_norm=clip)
     o_t, o_scale, o_good = 0, loss_scale, 0
@@ -329,3 +330,72 @@ def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, ou
         compare_state(state_to_numpy(opt.state()), ref, exact=clip == 0.0, tag=f"step {step} ")
     if skip:
         assert o_t == 2
+
+
+
+@pytest.mark.parametrize("N,dtype,skip,clip,out_of_place,bucket", [
+    (4, "bf16", True, 0.0, False, 0),          # two passes because of the in-place skip
+    (8, "bf16", False, 0.0, True, 400_000),     # forced to two passes by the host shard
+    (4, "fp32", False, 0.5, True, 0),           # clip
+])
+def test_gradient_shard_in_host_memory(zero_lib, oracle_mod, N, dtype, skip, clip, out_of_place,
+                                       bucket):
+    """The owner's FP32 combined gradient kept in pinned host memory and reached
+    over the host link: the same step, bit for bit (within the clip tolerance)."""
+    run_parity(zero_lib, oracle_mod, N=N, psi=PSI_MULTI_SWEEP if N == 8 else PSI_SMALL,
+               dtype=dtype, skip=skip, clip=clip, out_of_place=out_of_place, bucket=bucket,
+               steps=3, bad_step=2 if skip else 0, loss_scale=512.0, dynamic=skip,
+               host_accum=True)
+
+
+def test_host_shard_accumulation_through_two_slots(zero_lib, oracle_mod):
+    """Gradients in pinned host memory stream through two device slots; each
+    reduced bucket is added to the owner's FP32 shard in host memory; the GPU
+    keeps no gradient shard (the offloaded-shard pattern with two buffers)."""
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    N, psi, bucket = 8, PSI_MULTI_SWEEP, 400_000
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(21)) * 0.02
+    opt = ZeroAdam(psi_pad, N, "bf16", bucket_elems=bucket, skip_on_overflow=True,
+                   out_of_place=True, loss_scale=1024.0, device=dev, master=master.to(dev),
+                   host_grad_accum=True)
+    assert opt.ws_bytes == zero_lib.ZERO_WORKSPACE_CONTROL_BYTES
+    slots = opt.make_slots()
+    copy_stream = torch.cuda.Stream(dev)
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams()
+    for step in (1, 2):
+        grads = _make_grads(N, psi, psi_pad, "bf16", 1e-3 * 1024.0, 77 + step)
+        host = [g.pin_memory() for g in grads]
+        opt.enqueue_from_host(host, slots, copy_stream)
+        res = opt.finish()
+        ores = oracle_mod.zero_step([_np(g) for g in grads], ref["master"], ref["m"], ref["v"],
+                                    ref["w"], hp, step, 1024.0, True)
+        compare_result(res, ores)
+        compare_state(state_to_numpy(opt.state()), ref, exact=True, tag=f"step {step} ")
+        # the host shard holds this step's combined gradient
+        g_host = opt.grad_accum.numpy()
+        g_ref = oracle_mod.all_reduce([_np(g) for g in grads], psi_pad, np.float32(1 / (8 * 1024.0)))
+        assert np.array_equal(g_host.view(np.uint32), g_ref.view(np.uint32))
+
+
+def test_host_shard_gradient_accumulation(zero_lib, oracle_mod):
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    N, k, psi = 4, 3, PSI_SMALL
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(5)) * 0.02
+    opt = ZeroAdam(psi_pad, N, "bf16", bucket_elems=65_536, device=dev, master=master.to(dev),
+                   micro_batches=k, host_grad_accum=True)
+    ref = _oracle_state(master.numpy())
+    for step in (1, 2):
+        micro = [_make_grads(N, psi, psi_pad, "bf16", 1e-3, 300 * step + mb) for mb in range(k)]
+        res = opt.step_accumulated([[g.to(dev) for g in mb] for mb in micro])
+        ores = oracle_mod.zero_step_accum([[_np(g) for g in mb] for mb in micro], ref["master"],
+                                          ref["m"], ref["v"], ref["w"], oracle_mod.Hparams(),
+                                          step, 1.0, False)
+        compare_result(res, ores)
+        compare_state(state_to_numpy(opt.state()), ref, exact=True, tag=f"step {step} ")

@@ -62,6 +62,7 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 static_assert(kGradOffset % 256 == 0, "gradient workspace alignment");
+static_assert(kGradOffset == ZERO_WORKSPACE_CONTROL_BYTES, "header's control-part size");
 
 // Per-step FP32 scalars, each rounded once from FP64.
 struct Scalars {
@@ -667,7 +668,12 @@ int written_spans(const zero_plan* p, Span* out) {
     add(p->dst_m, 4 * n);
     add(p->dst_v, 4 * n);
     add(p->dst_w_bf16, 2 * n);
-    add(p->workspace, workspace_bytes(p->psi_pad, &p->hp, p->in_place != 0));
+    if (p->grad_accum != nullptr) {
+        add(p->workspace, kGradOffset);
+        add(p->grad_accum, 4 * n);
+    } else {
+        add(p->workspace, workspace_bytes(p->psi_pad, &p->hp, p->in_place != 0));
+    }
     return k;
 }
 
@@ -683,7 +689,7 @@ StepArgs base_args(const zero_plan* p) {
     a.dst_m = p->dst_m;
     a.dst_v = p->dst_v;
     a.dst_w = p->dst_w_bf16;
-    a.gws = reinterpret_cast<float*>(ws + kGradOffset);
+    a.gws = p->grad_accum != nullptr ? p->grad_accum : reinterpret_cast<float*>(ws + kGradOffset);
     a.partials = reinterpret_cast<double*>(ws + kPartialsOffset);
     a.ctrl = reinterpret_cast<Ctrl*>(ws);
     a.s = make_scalars(&p->hp, p->N, p->loss_scale);
@@ -698,7 +704,7 @@ int plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
               const uint16_t* src_w, float* dst_master, float* dst_m, float* dst_v,
               uint16_t* dst_w, int64_t psi_pad, int32_t N, const zero_adam_hparams* hp,
               float loss_scale, void* workspace, size_t workspace_bytes_given,
-              bool allow_null_grads) {
+              bool allow_null_grads, float* grad_accum = nullptr) {
     if (plan == nullptr) return ZERO_ERR_ARG;
     const bool in_place = (dst_master == src_master);
     if (grads == nullptr || N < 1 || N > ZERO_MAX_RANKS || psi_pad < 0 ||
@@ -719,7 +725,18 @@ int plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
     for (const void* p : bufs)
         if (!aligned(p, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
     if (!aligned(src_w, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
-    const size_t need = workspace_bytes(psi_pad, hp, in_place);
+    float* accum_dev = nullptr;  // grad_accum as the device addresses it
+    if (grad_accum != nullptr) {
+        if (!aligned(grad_accum, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, grad_accum) != cudaSuccess ||
+            attr.devicePointer == nullptr) {
+            cudaGetLastError();  // clear the error that query may leave behind
+            return ZERO_ERR_ARG;
+        }
+        accum_dev = static_cast<float*>(attr.devicePointer);
+    }
+    const size_t need = grad_accum != nullptr ? kGradOffset : workspace_bytes(psi_pad, hp, in_place);
     if (workspace == nullptr || workspace_bytes_given < need || !aligned(workspace, 256))
         return ZERO_ERR_WORKSPACE;
 
@@ -742,12 +759,13 @@ int plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
     p.grad_dtype = grad_dtype;
     p.N = N;
     p.in_place = in_place ? 1 : 0;
-    p.two_pass = needs_two_passes(hp, in_place) ? 1 : 0;
+    p.two_pass = (needs_two_passes(hp, in_place) || grad_accum != nullptr) ? 1 : 0;
+    p.grad_accum = accum_dev;
     p.state = 1;
 
     if (have_data) {
         const uintptr_t n = static_cast<uintptr_t>(psi_pad);
-        Span sp[ZERO_MAX_RANKS + 9];
+        Span sp[ZERO_MAX_RANKS + 12];  // grads + up to 6 written + 4 read-only
         int k = written_spans(&p, sp);
         auto add = [&](const void* ptr, uintptr_t bytes) {
             if (ptr != nullptr)
@@ -786,7 +804,7 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
         return ZERO_ERR_ARG;
     StepArgs a = base_args(p);
     if (bucket_grads != nullptr) {
-        Span written[5];
+        Span written[6];
         const int nw = written_spans(p, written);
         const uintptr_t bytes = static_cast<uintptr_t>(end - begin) * grad_elem_bytes(p->grad_dtype);
         for (int i = 0; i < p->N; ++i) {
@@ -946,6 +964,18 @@ extern "C" int zero_plan_init(zero_plan* plan, const void* const* grads, int32_t
     return plan_init(plan, grads, grad_dtype, src_master, src_m, src_v, src_w_bf16, dst_master,
                      dst_m, dst_v, dst_w_bf16, psi_pad, N, hp, loss_scale, workspace,
                      workspace_bytes_given, true);
+}
+
+extern "C" int zero_plan_init_ex(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
+                                 const float* src_master, const float* src_m, const float* src_v,
+                                 const uint16_t* src_w_bf16, float* dst_master, float* dst_m,
+                                 float* dst_v, uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
+                                 const zero_adam_hparams* hp, float loss_scale, void* workspace,
+                                 size_t workspace_bytes_given, float* grad_accum) {
+    if (psi_pad > 0 && (src_master == nullptr || dst_master == nullptr)) return ZERO_ERR_ARG;
+    return plan_init(plan, grads, grad_dtype, src_master, src_m, src_v, src_w_bf16, dst_master,
+                     dst_m, dst_v, dst_w_bf16, psi_pad, N, hp, loss_scale, workspace,
+                     workspace_bytes_given, true, grad_accum);
 }
 
 extern "C" int zero_plan_begin(zero_plan* plan, void* stream) { return plan_begin(plan, stream); }

@@ -59,7 +59,8 @@ class ZeroAdam:
                  beta2=0.999, eps=1e-8, weight_decay=0.0, max_grad_norm=0.0,
                  skip_on_overflow=False, bucket_elems=0, loss_scale=1.0,
                  dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
-                 device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0):
+                 device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0,
+                 host_grad_accum: bool = False):
         self.psi_pad, self.N = psi_pad, N
         self.grad_dtype = Z.ZERO_GRAD_BF16 if grad_dtype == "bf16" else Z.ZERO_GRAD_FP32
         self.hp = Z.make_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1,
@@ -80,7 +81,13 @@ class ZeroAdam:
                 "w": torch.zeros(psi_pad, dtype=torch.int16, device=self.device),
             })
         self.cur = 0
-        self.ws_bytes = Z.zero_workspace_bytes(psi_pad, self.hp, not out_of_place)
+        # host_grad_accum: the owner's FP32 gradient shard (or accumulator) lives
+        # in pinned host memory and the kernels reach it over the host link;
+        # steps then go through the plan entry points
+        self.grad_accum = (torch.zeros(psi_pad, dtype=torch.float32, pin_memory=True)
+                           if host_grad_accum else None)
+        self.ws_bytes = (Z.ZERO_WORKSPACE_CONTROL_BYTES if host_grad_accum else
+                         Z.zero_workspace_bytes(psi_pad, self.hp, not out_of_place))
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.result_t = torch.zeros(4, dtype=torch.int32, pin_memory=True)
         self.last = None
@@ -113,7 +120,7 @@ class ZeroAdam:
             keep them from overlapping."""
         self.hp.step = self.t + 1
         src = self._bufs[self.cur]
-        if api == "plan":
+        if api == "plan" or self.grad_accum is not None:
             return self._enqueue_plan(grads, src, stream, bucket_events, span_events)
         if self.out_of_place:
             dst = self._bufs[1 - self.cur]
@@ -137,10 +144,11 @@ class ZeroAdam:
     def _enqueue_plan(self, grads, src, stream, bucket_events, span_events=None) -> int:
         dst = self._bufs[1 - self.cur] if self.out_of_place else src
         plan = Z.zero_plan()
-        Z.check(Z.zero_plan_init(plan, grads, self.grad_dtype, src["master"], src["m"], src["v"],
-                                 src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
-                                 self.psi_pad, self.N, self.hp, self.scaler.scale, self.workspace,
-                                 self.ws_bytes), "zero_plan_init")
+        Z.check(Z.zero_plan_init_ex(plan, grads, self.grad_dtype, src["master"], src["m"],
+                                    src["v"], src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
+                                    self.psi_pad, self.N, self.hp, self.scaler.scale,
+                                    self.workspace, self.ws_bytes, self.grad_accum),
+                "zero_plan_init")
         # nothing but bucket launches goes between the buckets unless events
         # are recorded around each one
         plan.overlap_buckets = 0 if bucket_events is not None else 1
@@ -178,10 +186,11 @@ class ZeroAdam:
         src = self._bufs[self.cur]
         dst = self._bufs[1 - self.cur] if self.out_of_place else src
         plan = Z.zero_plan()
-        Z.check(Z.zero_plan_init(plan, micro_grads[0], self.grad_dtype, src["master"], src["m"],
-                                 src["v"], src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
-                                 self.psi_pad, self.N, self.hp, self.scaler.scale,
-                                 self.workspace, self.ws_bytes), "zero_plan_init")
+        Z.check(Z.zero_plan_init_ex(plan, micro_grads[0], self.grad_dtype, src["master"],
+                                    src["m"], src["v"], src["w"], dst["master"], dst["m"],
+                                    dst["v"], dst["w"], self.psi_pad, self.N, self.hp,
+                                    self.scaler.scale, self.workspace, self.ws_bytes,
+                                    self.grad_accum), "zero_plan_init")
         plan.overlap_buckets = 1
         Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -223,10 +232,11 @@ class ZeroAdam:
         dst = self._bufs[1 - self.cur] if self.out_of_place else src
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         plan = Z.zero_plan()
-        Z.check(Z.zero_plan_init(plan, [None] * self.N, self.grad_dtype, src["master"], src["m"],
-                                 src["v"], src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
-                                 self.psi_pad, self.N, self.hp, self.scaler.scale,
-                                 self.workspace, self.ws_bytes), "zero_plan_init")
+        Z.check(Z.zero_plan_init_ex(plan, [None] * self.N, self.grad_dtype, src["master"],
+                                    src["m"], src["v"], src["w"], dst["master"], dst["m"],
+                                    dst["v"], dst["w"], self.psi_pad, self.N, self.hp,
+                                    self.scaler.scale, self.workspace, self.ws_bytes,
+                                    self.grad_accum), "zero_plan_init")
         Z.check(Z.zero_plan_begin(plan, s), "zero_plan_begin")
         if not hasattr(self, "_slot_events"):
             # freed[k] is recorded after the last read of slot k, also across steps

@@ -40,6 +40,7 @@ ZERO_ERR_WORKSPACE = -5
 ZERO_ERR_OVERLAP = -6
 ZERO_ERR_TOO_LARGE = -7
 
+ZERO_WORKSPACE_CONTROL_BYTES = 16640
 ZERO_NOALLOC_MAX_TWO_PASS_ELEMS = 4194304
 ZERO_NOALLOC_SCRATCH_BYTES = 16640 + 4 * ZERO_NOALLOC_MAX_TWO_PASS_ELEMS
 
@@ -71,7 +72,8 @@ class zero_plan(ctypes.Structure):
                 ("src_w_bf16", ctypes.c_void_p), ("dst_master", ctypes.c_void_p),
                 ("dst_m", ctypes.c_void_p), ("dst_v", ctypes.c_void_p),
                 ("dst_w_bf16", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("psi_pad", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t), ("grad_accum", ctypes.c_void_p),
+                ("psi_pad", ctypes.c_int64),
                 ("cursor", ctypes.c_int64), ("hp", zero_adam_hparams),
                 ("loss_scale", ctypes.c_float), ("grad_dtype", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("in_place", ctypes.c_int32), ("two_pass", ctypes.c_int32),
@@ -100,6 +102,9 @@ _lib.zero_step_into.restype = ctypes.c_int
 _lib.zero_plan_init.argtypes = [_PLAN, _P, _i32, _P, _P, _P, _P, _P, _P, _P, _P, _i64, _i32,
                                 ctypes.POINTER(zero_adam_hparams), _f32, _P, ctypes.c_size_t]
 _lib.zero_plan_init.restype = ctypes.c_int
+_lib.zero_plan_init_ex.argtypes = [_PLAN, _P, _i32, _P, _P, _P, _P, _P, _P, _P, _P, _i64, _i32,
+                                   ctypes.POINTER(zero_adam_hparams), _f32, _P, ctypes.c_size_t, _P]
+_lib.zero_plan_init_ex.restype = ctypes.c_int
 _lib.zero_plan_begin.argtypes = [_PLAN, _P]
 _lib.zero_plan_begin.restype = ctypes.c_int
 _lib.zero_plan_bucket.argtypes = [_PLAN, _i64, _i64, _P, _P]
@@ -220,6 +225,18 @@ def zero_plan_init(plan: zero_plan, grads, grad_dtype: int, src_master, src_m, s
                                workspace_bytes)
 
 
+def zero_plan_init_ex(plan: zero_plan, grads, grad_dtype: int, src_master, src_m, src_v,
+                      src_w_bf16, dst_master, dst_m, dst_v, dst_w_bf16, psi_pad: int, N: int,
+                      hp: zero_adam_hparams, loss_scale: float, workspace, workspace_bytes: int,
+                      grad_accum=None) -> int:
+    return _lib.zero_plan_init_ex(ctypes.byref(plan), _grad_array(grads), grad_dtype,
+                                  _addr(src_master), _addr(src_m), _addr(src_v),
+                                  _addr(src_w_bf16), _addr(dst_master), _addr(dst_m),
+                                  _addr(dst_v), _addr(dst_w_bf16), psi_pad, N, ctypes.byref(hp),
+                                  loss_scale, _addr(workspace), workspace_bytes,
+                                  _addr(grad_accum))
+
+
 def zero_plan_begin(plan: zero_plan, stream=None) -> int:
     return _lib.zero_plan_begin(ctypes.byref(plan), _stream(stream))
 
@@ -275,6 +292,7 @@ def zero_launch_count() -> int:
 def exported_symbols() -> list[str]:
     """Names of the C functions this binding expects the library to export."""
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
-            "zero_step_into", "zero_plan_init", "zero_plan_begin", "zero_plan_bucket",
+            "zero_step_into", "zero_plan_init", "zero_plan_init_ex", "zero_plan_begin",
+            "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
             "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes"]
