@@ -67,6 +67,11 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = min(steps, 10)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--policy", choices=["auto", "host", "device"], default="auto",
+                    help="where t and the loss scale are kept: 'device' runs steps back to "
+                         "back with no host read in between; 'auto' picks the device when the "
+                         "workload skips on overflow or has a dynamic loss scale (otherwise "
+                         "no step outcome is needed on the host anyway)")
     ap.add_argument("--host-grad-accum", action="store_true",
                     help="keep the owner's FP32 gradient shard in pinned host memory "
                          "(reached over the host link); forces the two-pass form")
@@ -275,6 +280,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     wl = select_workload(args)
     out_of_place = not args.in_place
+    device_policy = args.policy == "device" or (
+        args.policy == "auto" and (wl.skip_on_overflow or wl.dynamic_loss_scale))
     grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
     # the end-to-end leg's pinned host copy of the gradients, made before the
     # large device allocations as an application would hold it from the start
@@ -285,7 +292,8 @@ def run_ours(args, world, rank, local):
                    skip_on_overflow=wl.skip_on_overflow, bucket_elems=wl.bucket_elems,
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
                    out_of_place=out_of_place, device=dev, master=master,
-                   micro_batches=args.micro_batches, host_grad_accum=args.host_grad_accum)
+                   micro_batches=args.micro_batches, host_grad_accum=args.host_grad_accum,
+                   device_policy=device_policy)
     buckets = opt.bucket_bounds()
     k_micro = max(1, args.micro_batches)
     # One event pair per step around its sequence of first-pass launches.
@@ -400,6 +408,7 @@ def run_ours(args, world, rank, local):
                    "skip_on_overflow": wl.skip_on_overflow, "max_grad_norm": wl.max_grad_norm,
                    "micro_batches": k_micro,
                    "grad_shard": "pinned host memory" if args.host_grad_accum else "HBM",
+                   "step_policy": "device" if device_policy else "host",
                    "entry": ("zero_plan_* (= zero_step_into)" if args.api == "plan"
                              else "zero_step_into") if out_of_place else
                    ("zero_plan_* (= zero_step)" if args.api == "plan" else "zero_step"),

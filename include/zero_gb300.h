@@ -74,8 +74,10 @@ typedef enum {
     ZERO_ERR_TIMEOUT = -4,    /* a bounded wait inside a kernel gave up            */
     ZERO_ERR_WORKSPACE = -5,  /* workspace missing, too small or misaligned        */
     ZERO_ERR_OVERLAP = -6,    /* two buffers that must be disjoint overlap         */
-    ZERO_ERR_TOO_LARGE = -7   /* the step needs more scratch than zero_step_noalloc's
+    ZERO_ERR_TOO_LARGE = -7,  /* the step needs more scratch than zero_step_noalloc's
                                  fixed array holds                                 */
+    ZERO_ERR_POLICY_WINDOW = -8 /* device policy: the step's t fell outside the window
+                                 of bias corrections it was given; nothing changed  */
 } zero_status;
 
 typedef enum {
@@ -253,6 +255,9 @@ typedef struct {
     int32_t two_pass;                  /* 1 if the update waits for a second pass          */
     int32_t state;                     /* 0 unset, 1 initialised, 2 begun                 */
     int32_t micro_batch;               /* micro-batch the next bucket belongs to          */
+    int32_t policy_t_count;            /* device policy: size of the t window (0 = none)   */
+    int64_t policy_t_first;            /* device policy: first t of the window            */
+    void* policy;                      /* device policy (zero_plan_set_device_policy)     */
     int32_t overlap_buckets;           /* 0 (as zero_plan_init leaves it): every bucket
                                           launch waits for all work before it on the
                                           stream.  1: the caller promises to enqueue
@@ -298,6 +303,45 @@ int zero_plan_init_ex(zero_plan* plan, const void* const* grads, int32_t grad_dt
                       uint16_t* dst_w_bf16, int64_t psi_pad, int32_t N,
                       const zero_adam_hparams* hp, float loss_scale, void* workspace,
                       size_t workspace_bytes, float* grad_accum);
+
+/* ------------------------------------------------------------------------
+ * Device-resident step policy.  The host normally has to read each step's
+ * outcome before it can issue the next step: a skipped step leaves t where it
+ * was, and the dynamic loss scale reacts to overflow.  With a device policy
+ * that bookkeeping stays on the GPU, so the host can issue steps back to back
+ * without waiting for any of them.  (Not on the pages; the host-side policy
+ * is the same rule.)
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int64_t t;                 /* steps applied so far; the next applied step uses t + 1 */
+    float loss_scale;          /* the scale the next step's gradients carry             */
+    int32_t good_steps;        /* clean steps since the scale last changed              */
+    int32_t growth_interval;   /* > 0: the scale grows after that many clean steps and
+                                  backs off after an overflowing one; 0: static scale   */
+    float backoff;             /* e.g. 0.5                                              */
+    float growth;              /* e.g. 2.0                                              */
+    int32_t last_status;       /* status of the latest step (as zero_step_result.status) */
+} zero_device_policy;
+
+#define ZERO_POLICY_WINDOW 16   /* most t values one step can be given */
+
+/* Makes the plan's step take t and the loss scale from *policy instead of
+ * hp->step and the loss_scale argument.  *policy is caller-owned and
+ * device-addressable: device memory, or pinned host memory the host may read
+ * at any time.  When the step ends, the device updates *policy:
+ *   - t advances if the step applied;
+ *   - with growth_interval > 0, an overflowing step multiplies the scale by
+ *     backoff and restarts good_steps; otherwise good_steps counts up and, on
+ *     reaching growth_interval, multiplies the scale by growth and restarts;
+ *   - last_status is set.
+ * The step uses t' = policy->t + 1 at its start.  The bias corrections depend
+ * on t', and the host, which may not know t' yet, computes them for every t'
+ * in [t_first, t_first + t_count), with 1 <= t_count <= ZERO_POLICY_WINDOW.
+ * If t' falls outside that window the step changes nothing and ends with
+ * status ZERO_ERR_POLICY_WINDOW.  Call between zero_plan_init(_ex) and
+ * zero_plan_begin.  Returns ZERO_OK or ZERO_ERR_ARG. */
+int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* policy, int64_t t_first,
+                                int32_t t_count);
 
 /* Starts the step: clears the control block on `stream`. */
 int zero_plan_begin(zero_plan* plan, void* stream);

@@ -197,7 +197,8 @@ def test_struct_layouts_match_the_header(zero_lib, tmp_path):
     import subprocess
     src = tmp_path / "layout.c"
     structs = {"zero_layout": zero_lib.zero_layout, "zero_adam_hparams": zero_lib.zero_adam_hparams,
-               "zero_step_result": zero_lib.zero_step_result, "zero_plan": zero_lib.zero_plan}
+               "zero_step_result": zero_lib.zero_step_result, "zero_plan": zero_lib.zero_plan,
+               "zero_device_policy": zero_lib.zero_device_policy}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "zero_gb300.h"',
              "int main(void) {"]
     for name, cls in structs.items():

@@ -399,3 +399,97 @@ def test_host_shard_gradient_accumulation(zero_lib, oracle_mod):
                                           step, 1.0, False)
         compare_result(res, ores)
         compare_state(state_to_numpy(opt.state()), ref, exact=True, tag=f"step {step} ")
+
+
+def _policy_run(zero_lib, oracle_mod, *, out_of_place, skip, bad_steps, steps, async_steps,
+                N=4, psi=PSI_SMALL, clip=0.0):
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(8)) * 0.02
+    opt = ZeroAdam(psi_pad, N, "bf16", skip_on_overflow=skip, max_grad_norm=clip,
+                   loss_scale=4096.0, dynamic_loss_scale=True, growth_interval=2,
+                   out_of_place=out_of_place, device=dev, master=master.to(dev),
+                   device_policy=True)
+    assert not opt.needs_result
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams(max_grad_norm=clip)
+    o_t, o_scale, o_good = 0, 4096.0, 0
+    all_grads = []
+    for step in range(1, steps + 1):
+        # every step's gradients are drawn at the oracle's running scale, which
+        # the device policy must track too
+        grads = _make_grads(N, psi, psi_pad, "bf16", 1e-3 * o_scale, 900 + step)
+        if step in bad_steps:
+            grads[1][4321] = float("inf")
+        all_grads.append(grads)
+        ores = oracle_mod.zero_step([_np(g) for g in grads], ref["master"], ref["m"], ref["v"],
+                                    ref["w"], hp, o_t + 1, o_scale, skip)
+        if ores["applied"]:
+            o_t += 1
+        o_scale, o_good = oracle_mod.loss_scale_update(o_scale, o_good, ores["found_nonfinite"],
+                                                       2, 0.5, 2.0)
+    dev_grads = [[g.to(dev) for g in gs] for gs in all_grads]
+    torch.cuda.synchronize()
+    for step, gs in enumerate(dev_grads, start=1):
+        if async_steps:
+            assert opt.step_async(gs) is None
+        else:
+            opt.step(gs)
+    res = opt.finish()
+    assert res["status"] in (zero_lib.ZERO_OK, zero_lib.ZERO_STEP_SKIPPED)
+    assert opt.t == o_t and opt.scaler.scale == o_scale
+    compare_state(state_to_numpy(opt.state()), ref, exact=clip == 0.0)
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+@pytest.mark.parametrize("async_steps", [False, True])
+def test_device_policy_tracks_the_host_rule(zero_lib, oracle_mod, out_of_place, async_steps):
+    """t and the dynamic loss scale kept on the device: steps issued with
+    (step by step) or without (back to back) host reads give the oracle's
+    state, t and scale; steps 3 and 4 overflow and are skipped."""
+    _policy_run(zero_lib, oracle_mod, out_of_place=out_of_place, skip=True, bad_steps={3, 4},
+                steps=7, async_steps=async_steps)
+
+
+def test_device_policy_with_clip(zero_lib, oracle_mod):
+    _policy_run(zero_lib, oracle_mod, out_of_place=True, skip=True, bad_steps={2}, steps=4,
+                async_steps=True, clip=0.05)
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_device_policy_window_miss_changes_nothing(zero_lib, out_of_place):
+    """A step whose device t falls outside the window it was given leaves the
+    state untouched (a copy of it, out of place) and reports the miss."""
+    import ctypes
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, n = 4, 4 * 128 * 64
+    grads = [(torch.randn(n, generator=torch.Generator().manual_seed(i)) * 1e-3).to(
+        torch.bfloat16).to(dev) for i in range(N)]
+    src = [torch.randn(n, device=dev) * 0.02, torch.rand(n, device=dev) * 1e-4,
+           torch.rand(n, device=dev) * 1e-6, torch.zeros(n, dtype=torch.int16, device=dev)]
+    before = [t.clone() for t in src]
+    dst = [torch.full_like(t, 7) for t in src] if out_of_place else src
+    hp = Z.make_hparams(skip_on_overflow=False)
+    ws = torch.empty(Z.zero_workspace_bytes(n, hp, not out_of_place), dtype=torch.uint8,
+                     device=dev)
+    pol_mem = torch.zeros(ctypes.sizeof(Z.zero_device_policy), dtype=torch.uint8, pin_memory=True)
+    pol = Z.zero_device_policy.from_address(pol_mem.data_ptr())
+    pol.t, pol.loss_scale = 5, 1.0
+    res = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+    plan = Z.zero_plan()
+    assert Z.zero_plan_init(plan, grads, Z.ZERO_GRAD_BF16, *src, *dst, n, N, hp, 1.0, ws,
+                            ws.numel()) == Z.ZERO_OK
+    assert Z.zero_plan_set_device_policy(plan, pol_mem, 1, 3) == Z.ZERO_OK   # t' = 6 is outside
+    assert Z.zero_plan_begin(plan, None) == Z.ZERO_OK
+    assert Z.zero_plan_bucket(plan, 0, n, None, None) == Z.ZERO_OK
+    assert Z.zero_plan_end(plan, res, None) == Z.ZERO_OK
+    torch.cuda.synchronize()
+    assert int(res[0]) == Z.ZERO_ERR_POLICY_WINDOW
+    assert pol.t == 5 and pol.last_status == Z.ZERO_ERR_POLICY_WINDOW
+    for a, b in zip(dst, before):
+        assert torch.equal(a, b)
+    for a, b in zip(src, before):
+        assert torch.equal(a, b)

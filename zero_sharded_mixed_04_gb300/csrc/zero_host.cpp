@@ -107,6 +107,8 @@ extern "C" const char* zero_status_str(int status) {
         case ZERO_ERR_TIMEOUT: return "bounded wait inside a kernel timed out";
         case ZERO_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case ZERO_ERR_OVERLAP: return "buffers that must be disjoint overlap";
+        case ZERO_ERR_POLICY_WINDOW:
+            return "device policy: the step's t fell outside its window of bias corrections";
         case ZERO_ERR_TOO_LARGE:
             return "step needs more scratch than the no-allocation entry point's fixed array";
         default: return "unknown status";

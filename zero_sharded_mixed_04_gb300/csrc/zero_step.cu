@@ -51,19 +51,6 @@ constexpr size_t kGradOffset = kPartialsOffset + kMaxGrid * sizeof(double);  // 
 
 std::atomic<uint64_t> g_launches{0};
 
-// Control block at the start of the workspace.  It is zeroed at the start of
-// every step.
-struct Ctrl {
-    unsigned int nonfinite;    // OR over all elements of "combined gradient is inf/NaN"
-    int skip;                  // decided by the finalize kernel
-    float clip_coef;           // decided by the finalize kernel
-    float grad_norm;
-    zero_step_result result;   // the outcome, when the caller passes no result pointer
-};
-static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
-static_assert(kGradOffset % 256 == 0, "gradient workspace alignment");
-static_assert(kGradOffset == ZERO_WORKSPACE_CONTROL_BYTES, "header's control-part size");
-
 // Per-step FP32 scalars, each rounded once from FP64.
 struct Scalars {
     float inv;        // 1 / (N * loss_scale)
@@ -76,6 +63,21 @@ struct Scalars {
     int use_decay;
 };
 
+// Control block at the start of the workspace.  It is zeroed at the start of
+// every step.
+struct Ctrl {
+    unsigned int nonfinite;    // OR over all elements of "combined gradient is inf/NaN"
+    int skip;                  // decided by the finalize kernel
+    float clip_coef;           // decided by the finalize kernel
+    float grad_norm;
+    zero_step_result result;   // the outcome, when the caller passes no result pointer
+    int policy_error;          // device policy: t fell outside the given window
+    Scalars scalars;           // device policy: this step's scalars, set by the prologue
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+static_assert(kGradOffset % 256 == 0, "gradient workspace alignment");
+static_assert(kGradOffset == ZERO_WORKSPACE_CONTROL_BYTES, "header's control-part size");
+
 struct StepArgs {
     const void* grads[ZERO_MAX_RANKS];
     const float* src_master;
@@ -86,6 +88,7 @@ struct StepArgs {
     float* dst_m;
     float* dst_v;
     uint16_t* dst_w;
+    const Scalars* sdev; // device policy: read the step's scalars here instead of s
     float* gws;          // FP32 combined gradient (two-pass form)
     double* partials;    // one FP64 sum of squares per CTA
     Ctrl* ctrl;
@@ -98,6 +101,17 @@ struct StepArgs {
     int32_t acc_first;   // accumulation: this is the first micro-batch (start from +0)
     int32_t acc_last;    // accumulation: the last micro-batch (form the step-wide checks)
 };
+
+// The step's scalars: from the kernel arguments, or, under a device policy,
+// from the control block where the prologue kernel wrote them.
+__device__ __forceinline__ Scalars step_scalars(const StepArgs& a) {
+    return a.sdev != nullptr ? *a.sdev : a.s;
+}
+
+// Under a device policy a step whose t fell outside its window does nothing.
+__device__ __forceinline__ bool policy_off(const StepArgs& a) {
+    return a.sdev != nullptr && a.ctrl->policy_error != 0;
+}
 
 // ------------------------------------------------------------------ element math
 
@@ -254,8 +268,9 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 // src_*, writes dst_* (the same arrays for an in-place step).
 // One 8-element group: reduce-scatter + scale + check + Adam + BF16 all-gather.
 template <int NT, bool kBF16, int U>
-__device__ __forceinline__ void fused_groups(const StepArgs& a, const int64_t (&j)[U],
-                                             unsigned& bad, double& sumsq) {
+__device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s,
+                                             const int64_t (&j)[U], unsigned& bad,
+                                             double& sumsq) {
     float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
     // every load of the U groups is issued before any arithmetic
 #pragma unroll
@@ -271,10 +286,10 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const int64_t (&
         float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-            const float gs = __fmul_rn(g[u][e], a.s.inv);
+            const float gs = __fmul_rn(g[u][e], s.inv);
             bad |= is_nonfinite(gs) ? 1u : 0u;
             sq = fmaf(gs, gs, sq);
-            adam_element(gs, p[u][e], m[u][e], v[u][e], a.s);
+            adam_element(gs, p[u][e], m[u][e], v[u][e], s);
         }
         sumsq += static_cast<double>(sq);
     }
@@ -296,15 +311,17 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
     allow_next_launch();
     unsigned bad = 0;
     double sumsq = 0.0;
+    const Scalars s = step_scalars(a);
+    const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    for (; q + stride < a.n8; q += 2 * stride) {
+    for (; q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
-        fused_groups<NT, kBF16, 2>(a, j, bad, sumsq);
+        fused_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
     }
-    if (q < a.n8) {
+    if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        fused_groups<NT, kBF16, 1>(a, j, bad, sumsq);
+        fused_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -316,8 +333,10 @@ __global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_cons
     allow_next_launch();
     unsigned bad = 0;
     double sumsq = 0.0;
+    const Scalars s = step_scalars(a);
+    const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < n8;
          q += stride) {
         const int64_t j = a.begin + q * kVec;
         float g[kVec];
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_cons
         float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-            g[e] = __fmul_rn(g[e], a.s.inv);
+            g[e] = __fmul_rn(g[e], s.inv);
             bad |= is_nonfinite(g[e]) ? 1u : 0u;
             sq = fmaf(g[e], g[e], sq);
         }
@@ -345,8 +364,10 @@ __global__ void __launch_bounds__(kThreads) zero_accum_kernel(const __grid_const
     allow_next_launch();
     unsigned bad = 0;
     double sumsq = 0.0;
+    const Scalars s = step_scalars(a);
+    const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < n8;
          q += stride) {
         const int64_t j = a.begin + q * kVec;
         float acc[kVec], g[kVec];
@@ -360,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) zero_accum_kernel(const __grid_const
         float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-            acc[e] = __fadd_rn(acc[e], __fmul_rn(g[e], a.s.inv));
+            acc[e] = __fadd_rn(acc[e], __fmul_rn(g[e], s.inv));
             bad |= is_nonfinite(acc[e]) ? 1u : 0u;
             sq = fmaf(acc[e], acc[e], sq);
         }
@@ -396,6 +417,7 @@ __global__ void __launch_bounds__(kThreads) zero_update_kernel(const __grid_cons
         if (a.dst_master != a.src_master) copy_state(a);
     } else {
         const float coef = a.ctrl->clip_coef;
+        const Scalars s = step_scalars(a);
         const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
         for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
              q += stride) {
@@ -408,7 +430,7 @@ __global__ void __launch_bounds__(kThreads) zero_update_kernel(const __grid_cons
 #pragma unroll
             for (int e = 0; e < kVec; ++e) {
                 const float gs = a.clip ? __fmul_rn(g[e], coef) : g[e];
-                adam_element(gs, p[e], m[e], v[e], a.s);
+                adam_element(gs, p[e], m[e], v[e], s);
             }
             store8(a.dst_master, j, p);
             store8(a.dst_m, j, m);
@@ -431,7 +453,7 @@ __global__ void __launch_bounds__(kThreads) zero_restore_kernel(const __grid_con
 // norm and clip coefficient, decides the skip, and writes the result.
 __global__ void __launch_bounds__(kFinalizeThreads)
 zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int skip_on_overflow,
-                     zero_step_result* result) {
+                     zero_step_result* result, zero_device_policy* policy) {
     __shared__ double s[kFinalizeThreads];
     double t = 0.0;
     for (int i = threadIdx.x; i < kMaxGrid; i += kFinalizeThreads) t += partials[i];
@@ -445,7 +467,8 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         const double sumsq = s[0];
         const double norm = sqrt(sumsq);
         const int nonfinite = ctrl->nonfinite != 0u;
-        const int skip = (skip_on_overflow && nonfinite) ? 1 : 0;
+        const int window_miss = (policy != nullptr && ctrl->policy_error) ? 1 : 0;
+        const int skip = ((skip_on_overflow && nonfinite) || window_miss) ? 1 : 0;
         float coef = 1.0f;
         if (max_norm > 0.0 && !skip) {
             const double c = max_norm / (norm + 1e-6);
@@ -455,12 +478,55 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         ctrl->clip_coef = coef;
         ctrl->grad_norm = static_cast<float>(norm);
         zero_step_result r;
-        r.status = skip ? ZERO_STEP_SKIPPED : ZERO_OK;
+        r.status = window_miss ? ZERO_ERR_POLICY_WINDOW : (skip ? ZERO_STEP_SKIPPED : ZERO_OK);
         r.found_nonfinite = static_cast<uint32_t>(nonfinite);
         r.grad_norm = static_cast<float>(norm);
         r.clip_coef = coef;
         *result = r;
+        if (policy != nullptr) {
+            // the host-side rule, kept on the device: t counts applied steps;
+            // the dynamic scale backs off after an overflow, grows after
+            // growth_interval clean steps
+            if (!window_miss) {
+                if (!skip) policy->t += 1;
+                if (policy->growth_interval > 0) {
+                    if (nonfinite) {
+                        policy->loss_scale *= policy->backoff;
+                        policy->good_steps = 0;
+                    } else if (++policy->good_steps == policy->growth_interval) {
+                        policy->loss_scale *= policy->growth;
+                        policy->good_steps = 0;
+                    }
+                }
+            }
+            policy->last_status = r.status;
+            __threadfence_system();
+        }
     }
+}
+
+struct PolicyTable {
+    float step_size[ZERO_POLICY_WINDOW];  // lr / (1 - beta1^t) for t = t_first + i
+    float sbc2[ZERO_POLICY_WINDOW];       // sqrt(1 - beta2^t)
+};
+
+// Device policy, start of a step: picks the scalars for t' = policy->t + 1
+// from the host's window, forms the batch-mean factor from the device's loss
+// scale, and leaves them in the control block for the step's kernels.
+__global__ void zero_policy_prologue_kernel(const zero_device_policy* policy, Ctrl* ctrl,
+                                            Scalars base, PolicyTable table, int64_t t_first,
+                                            int32_t t_count, double ranks_times_micro) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const int64_t idx = policy->t + 1 - t_first;
+    Scalars s = base;
+    if (idx < 0 || idx >= t_count) {
+        ctrl->policy_error = 1;  // every kernel of the step then leaves the state alone
+    } else {
+        s.step_size = table.step_size[idx];
+        s.sbc2 = table.sbc2[idx];
+    }
+    s.inv = static_cast<float>(1.0 / (ranks_times_micro * static_cast<double>(policy->loss_scale)));
+    ctrl->scalars = s;
 }
 
 // ------------------------------------------------------------------ host side
@@ -693,6 +759,7 @@ StepArgs base_args(const zero_plan* p) {
     a.partials = reinterpret_cast<double*>(ws + kPartialsOffset);
     a.ctrl = reinterpret_cast<Ctrl*>(ws);
     a.s = make_scalars(&p->hp, p->N, p->loss_scale);
+    a.sdev = p->policy != nullptr ? &a.ctrl->scalars : nullptr;
     a.N = p->N;
     a.clip = p->hp.max_grad_norm > 0.0 ? 1 : 0;
     a.gbase = 0;
@@ -790,6 +857,23 @@ int plan_begin(zero_plan* p, void* stream) {
     if (cudaMemsetAsync(p->workspace, 0, kGradOffset, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return ZERO_ERR_CUDA;
+    if (p->policy != nullptr) {
+        PolicyTable table{};
+        zero_adam_hparams hp = p->hp;
+        for (int32_t i = 0; i < p->policy_t_count; ++i) {
+            hp.step = p->policy_t_first + i;
+            const Scalars si = make_scalars(&hp, p->N, p->loss_scale);
+            table.step_size[i] = si.step_size;
+            table.sbc2[i] = si.sbc2;
+        }
+        const Scalars base = make_scalars(&p->hp, p->N, p->loss_scale);
+        zero_policy_prologue_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+            static_cast<const zero_device_policy*>(p->policy),
+            reinterpret_cast<Ctrl*>(p->workspace), base, table, p->policy_t_first,
+            p->policy_t_count, static_cast<double>(p->N) * micro_batches_of(&p->hp));
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
+    }
     p->cursor = 0;
     p->micro_batch = 0;
     p->state = 2;
@@ -874,7 +958,8 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
     if (result_dev == nullptr) result_dev = &ctrl->result;
 
     zero_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(
-        ctrl, a.partials, p->hp.max_grad_norm, p->hp.skip_on_overflow, result_dev);
+        ctrl, a.partials, p->hp.max_grad_norm, p->hp.skip_on_overflow, result_dev,
+        static_cast<zero_device_policy*>(p->policy));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
 
@@ -882,7 +967,7 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
         // the first update launch waits for the finalize kernel in stream order
         if (!launch_range(zero_update_kernel, device, a, 0, p->psi_pad, stream, false))
             return ZERO_ERR_CUDA;
-    } else if (!p->in_place && p->hp.skip_on_overflow) {
+    } else if (!p->in_place && (p->hp.skip_on_overflow || p->policy != nullptr)) {
         a.begin = 0;
         a.n8 = p->psi_pad / kVec;
         if (!launch(zero_restore_kernel, device, a, stream)) return ZERO_ERR_CUDA;
@@ -976,6 +1061,25 @@ extern "C" int zero_plan_init_ex(zero_plan* plan, const void* const* grads, int3
     return plan_init(plan, grads, grad_dtype, src_master, src_m, src_v, src_w_bf16, dst_master,
                      dst_m, dst_v, dst_w_bf16, psi_pad, N, hp, loss_scale, workspace,
                      workspace_bytes_given, true, grad_accum);
+}
+
+extern "C" int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* policy,
+                                           int64_t t_first, int32_t t_count) {
+    if (plan == nullptr || plan->state != 1 || policy == nullptr || t_first < 1 || t_count < 1 ||
+        t_count > ZERO_POLICY_WINDOW || !aligned(policy, 8))
+        return ZERO_ERR_ARG;
+    // An in-place one-pass step cannot leave its state alone once it has run,
+    // so a window miss must be caught before: only the plan's kernels check
+    // it, and they all do.  The policy must be device-addressable.
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, policy) != cudaSuccess || attr.devicePointer == nullptr) {
+        cudaGetLastError();
+        return ZERO_ERR_ARG;
+    }
+    plan->policy = attr.devicePointer;
+    plan->policy_t_first = t_first;
+    plan->policy_t_count = t_count;
+    return ZERO_OK;
 }
 
 extern "C" int zero_plan_begin(zero_plan* plan, void* stream) { return plan_begin(plan, stream); }

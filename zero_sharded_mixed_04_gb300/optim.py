@@ -15,6 +15,8 @@ Every step runs in libzero_gb300.so; nothing here touches the data.
 """
 from __future__ import annotations
 
+import collections
+import ctypes
 from dataclasses import dataclass
 
 import torch
@@ -60,7 +62,7 @@ class ZeroAdam:
                  skip_on_overflow=False, bucket_elems=0, loss_scale=1.0,
                  dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
                  device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0,
-                 host_grad_accum: bool = False):
+                 host_grad_accum: bool = False, device_policy: bool = False):
         self.psi_pad, self.N = psi_pad, N
         self.grad_dtype = Z.ZERO_GRAD_BF16 if grad_dtype == "bf16" else Z.ZERO_GRAD_FP32
         self.hp = Z.make_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1,
@@ -89,6 +91,21 @@ class ZeroAdam:
         self.ws_bytes = (Z.ZERO_WORKSPACE_CONTROL_BYTES if host_grad_accum else
                          Z.zero_workspace_bytes(psi_pad, self.hp, not out_of_place))
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        # device_policy: t and the loss scale live in a zero_device_policy in
+        # pinned host memory that the device updates at the end of each step,
+        # so steps need no host read in between
+        self.policy_mem = None
+        if device_policy:
+            nbytes = ctypes.sizeof(Z.zero_device_policy)
+            self.policy_mem = torch.zeros(nbytes, dtype=torch.uint8, pin_memory=True)
+            self.policy = Z.zero_device_policy.from_address(self.policy_mem.data_ptr())
+            self.policy.t = 0
+            self.policy.loss_scale = loss_scale
+            self.policy.good_steps = 0
+            self.policy.growth_interval = growth_interval if dynamic_loss_scale else 0
+            self.policy.backoff = self.scaler.backoff
+            self.policy.growth = self.scaler.growth
+            self._inflight = collections.deque()
         self.result_t = torch.zeros(4, dtype=torch.int32, pin_memory=True)
         self.last = None
 
@@ -120,7 +137,7 @@ class ZeroAdam:
             keep them from overlapping."""
         self.hp.step = self.t + 1
         src = self._bufs[self.cur]
-        if api == "plan" or self.grad_accum is not None:
+        if api == "plan" or self.grad_accum is not None or self.policy_mem is not None:
             return self._enqueue_plan(grads, src, stream, bucket_events, span_events)
         if self.out_of_place:
             dst = self._bufs[1 - self.cur]
@@ -152,6 +169,7 @@ class ZeroAdam:
         # nothing but bucket launches goes between the buckets unless events
         # are recorded around each one
         plan.overlap_buckets = 0 if bucket_events is not None else 1
+        self._apply_policy(plan, stream)
         Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if span_events is not None:
@@ -168,6 +186,7 @@ class ZeroAdam:
         # kernel launches of the first pass (the library splits long ranges)
         self.first_pass_launches = Z.zero_launch_count() - n0
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
+        self._note_enqueued(s)
         if self.out_of_place:
             self.cur = 1 - self.cur
         return rc
@@ -192,6 +211,7 @@ class ZeroAdam:
                                     self.scaler.scale, self.workspace, self.ws_bytes,
                                     self.grad_accum), "zero_plan_init")
         plan.overlap_buckets = 1
+        self._apply_policy(plan, stream)
         Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if span_events is not None:
@@ -205,6 +225,7 @@ class ZeroAdam:
             span_events[1].record(s)
         self.first_pass_launches = Z.zero_launch_count() - n0
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
+        self._note_enqueued(s)
         if self.out_of_place:
             self.cur = 1 - self.cur
         return rc
@@ -237,6 +258,7 @@ class ZeroAdam:
                                     dst["v"], dst["w"], self.psi_pad, self.N, self.hp,
                                     self.scaler.scale, self.workspace, self.ws_bytes,
                                     self.grad_accum), "zero_plan_init")
+        self._apply_policy(plan, s)
         Z.check(Z.zero_plan_begin(plan, s), "zero_plan_begin")
         if not hasattr(self, "_slot_events"):
             # freed[k] is recorded after the last read of slot k, also across steps
@@ -256,9 +278,33 @@ class ZeroAdam:
             Z.check(Z.zero_plan_bucket(plan, b0, b1, slot, s), "zero_plan_bucket")
             freed[k % 2].record(s)
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, s), "zero_plan_end")
+        self._note_enqueued(s)
         if self.out_of_place:
             self.cur = 1 - self.cur
         return rc
+
+    def _apply_policy(self, plan, stream) -> None:
+        if self.policy_mem is not None:
+            t_first, t_count = self._policy_window(stream)
+            Z.check(Z.zero_plan_set_device_policy(plan, self.policy_mem, t_first, t_count),
+                    "zero_plan_set_device_policy")
+
+    def _note_enqueued(self, s) -> None:
+        if self.policy_mem is not None:
+            ev = torch.cuda.Event()
+            ev.record(s)
+            self._inflight.append(ev)
+
+    def _policy_window(self, stream=None) -> tuple[int, int]:
+        """The t values the next step may see on the device: from the policy's
+        t, read after the completed steps are known, up to one more per step
+        still in flight."""
+        while self._inflight and self._inflight[0].query():
+            self._inflight.popleft()
+        while len(self._inflight) >= Z.ZERO_POLICY_WINDOW - 1:
+            self._inflight.popleft().synchronize()
+        t_read = int(self.policy.t)
+        return t_read + 1, len(self._inflight) + 1
 
     def finish(self, stream=None) -> dict:
         """Wait for the last enqueued step, read its result and advance the
@@ -272,9 +318,15 @@ class ZeroAdam:
         coef = float(raw[3:4].view(torch.float32)[0])
         Z.check(status, "zero_step (device)")
         applied = status == Z.ZERO_OK
-        if applied:
-            self.t += 1
-        self.scaler.update(found)
+        if self.policy_mem is not None:
+            self._inflight.clear()               # the stream is idle
+            self.t = int(self.policy.t)
+            self.scaler.scale = float(self.policy.loss_scale)
+            self.scaler.good_steps = int(self.policy.good_steps)
+        else:
+            if applied:
+                self.t += 1
+            self.scaler.update(found)
         self.last = {"applied": applied, "found_nonfinite": found, "grad_norm": norm,
                      "clip_coef": coef, "status": status}
         return self.last
@@ -285,6 +337,8 @@ class ZeroAdam:
         It must when a step can be skipped (t then does not advance) or the
         loss scale reacts to overflow.  Otherwise every step applies and the
         host can run ahead of the device."""
+        if self.policy_mem is not None:
+            return False  # the device keeps t and the loss scale
         return bool(self.hp.skip_on_overflow) or self.scaler.dynamic
 
     def step_async(self, grads, stream=None, api: str = "step", span_events=None) -> dict | None:
@@ -294,7 +348,8 @@ class ZeroAdam:
         self.enqueue(grads, stream, api, None, span_events)
         if self.needs_result:
             return self.finish(stream)
-        self.t += 1
+        if self.policy_mem is None:
+            self.t += 1
         return None
 
     def last_result(self, stream=None) -> dict:

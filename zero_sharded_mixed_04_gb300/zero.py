@@ -39,6 +39,8 @@ ZERO_ERR_TIMEOUT = -4
 ZERO_ERR_WORKSPACE = -5
 ZERO_ERR_OVERLAP = -6
 ZERO_ERR_TOO_LARGE = -7
+ZERO_ERR_POLICY_WINDOW = -8
+ZERO_POLICY_WINDOW = 16
 
 ZERO_WORKSPACE_CONTROL_BYTES = 16640
 ZERO_NOALLOC_MAX_TWO_PASS_ELEMS = 4194304
@@ -78,7 +80,15 @@ class zero_plan(ctypes.Structure):
                 ("loss_scale", ctypes.c_float), ("grad_dtype", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("in_place", ctypes.c_int32), ("two_pass", ctypes.c_int32),
                 ("state", ctypes.c_int32), ("micro_batch", ctypes.c_int32),
-                ("overlap_buckets", ctypes.c_int32)]
+                ("policy_t_count", ctypes.c_int32), ("policy_t_first", ctypes.c_int64),
+                ("policy", ctypes.c_void_p), ("overlap_buckets", ctypes.c_int32)]
+
+
+class zero_device_policy(ctypes.Structure):
+    _fields_ = [("t", ctypes.c_int64), ("loss_scale", ctypes.c_float),
+                ("good_steps", ctypes.c_int32), ("growth_interval", ctypes.c_int32),
+                ("backoff", ctypes.c_float), ("growth", ctypes.c_float),
+                ("last_status", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -105,6 +115,8 @@ _lib.zero_plan_init.restype = ctypes.c_int
 _lib.zero_plan_init_ex.argtypes = [_PLAN, _P, _i32, _P, _P, _P, _P, _P, _P, _P, _P, _i64, _i32,
                                    ctypes.POINTER(zero_adam_hparams), _f32, _P, ctypes.c_size_t, _P]
 _lib.zero_plan_init_ex.restype = ctypes.c_int
+_lib.zero_plan_set_device_policy.argtypes = [_PLAN, _P, _i64, _i32]
+_lib.zero_plan_set_device_policy.restype = ctypes.c_int
 _lib.zero_plan_begin.argtypes = [_PLAN, _P]
 _lib.zero_plan_begin.restype = ctypes.c_int
 _lib.zero_plan_bucket.argtypes = [_PLAN, _i64, _i64, _P, _P]
@@ -237,6 +249,12 @@ def zero_plan_init_ex(plan: zero_plan, grads, grad_dtype: int, src_master, src_m
                                   _addr(grad_accum))
 
 
+def zero_plan_set_device_policy(plan: zero_plan, policy, t_first: int, t_count: int) -> int:
+    """policy: the address of a device-addressable zero_device_policy (a pinned
+    host tensor or device tensor of its size)."""
+    return _lib.zero_plan_set_device_policy(ctypes.byref(plan), _addr(policy), t_first, t_count)
+
+
 def zero_plan_begin(plan: zero_plan, stream=None) -> int:
     return _lib.zero_plan_begin(ctypes.byref(plan), _stream(stream))
 
@@ -292,7 +310,8 @@ def zero_launch_count() -> int:
 def exported_symbols() -> list[str]:
     """Names of the C functions this binding expects the library to export."""
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
-            "zero_step_into", "zero_plan_init", "zero_plan_init_ex", "zero_plan_begin",
+            "zero_step_into", "zero_plan_init", "zero_plan_init_ex",
+            "zero_plan_set_device_policy", "zero_plan_begin",
             "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
             "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes"]
