@@ -85,7 +85,8 @@ def _oracle_check(oracle_mod, grads, N, scale, psi_pad):
     return any(p[0] for p in parts), math.fsum(p[1] for p in parts)
 
 
-def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=None):
+def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=None,
+                  device_policy=False):
     from zero_sharded_mixed_04_gb300 import synth
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     wl = synth.WORKLOADS[name]
@@ -98,7 +99,8 @@ def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=
                    eps=wl.eps, weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm,
                    skip_on_overflow=wl.skip_on_overflow, bucket_elems=wl.bucket_elems,
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
-                   out_of_place=out_of_place, device=dev, master=master)
+                   out_of_place=out_of_place, device=dev, master=master,
+                   device_policy=device_policy)
     del master
     _free()
     hp = oracle_mod.Hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
@@ -168,3 +170,11 @@ def test_flat3b_n4_fp32(zero_lib, oracle_mod):
 
 def test_ragged6b_n4(zero_lib, oracle_mod):
     _run_workload(zero_lib, oracle_mod, "ragged6b_n4", out_of_place=False, full_compare=False)
+
+
+def test_flat1b_n8_as_benchmarked(zero_lib, oracle_mod):
+    """The path bench.py times: out of place, through the plan entry points,
+    with t and the loss scale kept on the device; the injected +inf on step 3
+    must be skipped and halve the scale there."""
+    _run_workload(zero_lib, oracle_mod, "flat1b_n8", out_of_place=True, full_compare=False,
+                  device_policy=True)

@@ -369,6 +369,41 @@ class ZeroAdam:
         return self.finish(stream)
 
 
+    # ---------------------------------------------------------------- checkpoint
+    def finish_pending(self) -> None:
+        """Wait for every enqueued step and bring t and the loss scale up to
+        date (with a device policy they live on the device)."""
+        torch.cuda.synchronize(self.device)
+        if self.policy_mem is not None:
+            self._inflight.clear()
+            self.t = int(self.policy.t)
+            self.scaler.scale = float(self.policy.loss_scale)
+            self.scaler.good_steps = int(self.policy.good_steps)
+
+    def state_dict(self) -> dict:
+        """Everything a later step depends on, on the host: the current
+        master/m/v and working weights, the step counter and the loss-scale
+        state."""
+        self.finish_pending()
+        st = self.state()
+        return {"master": st["master"].cpu(), "m": st["m"].cpu(), "v": st["v"].cpu(),
+                "w": st["w"].cpu(), "t": self.t, "loss_scale": self.scaler.scale,
+                "good_steps": self.scaler.good_steps, "psi_pad": self.psi_pad, "N": self.N}
+
+    def load_state_dict(self, sd: dict) -> None:
+        if sd["psi_pad"] != self.psi_pad or sd["N"] != self.N:
+            raise ValueError("checkpoint of a different layout")
+        self.finish_pending()
+        self.load_state(sd["master"], sd["m"], sd["v"], sd["w"])
+        self.t = int(sd["t"])
+        self.scaler.scale = float(sd["loss_scale"])
+        self.scaler.good_steps = int(sd["good_steps"])
+        if self.policy_mem is not None:
+            self.policy.t = self.t
+            self.policy.loss_scale = self.scaler.scale
+            self.policy.good_steps = self.scaler.good_steps
+
+
 class Zero3Views:
     """ZeRO-3 per-layer gather with two views: before layer i runs, layer i + 1
     is gathered into the other view on a side stream; a view is reused only
