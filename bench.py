@@ -285,7 +285,16 @@ def run_ours(args, world, rank, local):
     grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
     # the end-to-end leg's pinned host copy of the gradients, made before the
     # large device allocations as an application would hold it from the start
-    host_grads = None if args.no_e2e else pin_host_grads(grads)
+    host_grads, e2e_unavailable = None, None
+    if not args.no_e2e:
+        try:
+            host_grads = pin_host_grads(grads)
+        except RuntimeError as exc:  # not enough host memory to pin, say
+            e2e_unavailable = f"pinned host copy of the gradients failed: {exc}".splitlines()[0]
+        # every rank takes the same branch, since run_e2e holds barriers
+        if group.max(1.0 if e2e_unavailable else 0.0) > 0.0 and e2e_unavailable is None:
+            e2e_unavailable = "another rank could not pin its host copy of the gradients"
+            host_grads = None
     master = synth.make_master(wl, dev)
     opt = ZeroAdam(wl.psi_pad, wl.N, wl.grad_dtype, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
                    eps=wl.eps, weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm,
@@ -388,7 +397,9 @@ def run_ours(args, world, rank, local):
     step_gbs = b_alg * wl.psi_pad / (ms / 1e3) / 1e9
 
     e2e = None
-    if not args.no_e2e:
+    if e2e_unavailable is not None:
+        e2e = {"unavailable": e2e_unavailable}
+    elif not args.no_e2e:
         e2e = run_e2e(args, opt, grads, host_grads, wl, stream, dev, group)
 
     cpu = None
