@@ -311,15 +311,17 @@ def run_ours(args, world, rank, local):
     # scale) the host runs ahead of the device and the spans are read at the
     # end.
     stream = torch.cuda.current_stream(dev)
-    spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # with micro-batches a third event, recorded before the last micro-batch,
+    # splits the accumulate passes from the last one
+    n_ev = 3 if k_micro > 1 else 2
+    spans = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(n_ev))
              for _ in range(max(args.steps, args.warmup))]
 
     def one_step(k: int):
         ev = spans[k] if args.api == "plan" else None
         if k_micro > 1:
             # every micro-batch reads the same synthetic gradients
-            opt.enqueue_accumulated([grads] * k_micro, stream, span_events=ev)
-            res = opt.finish(stream)
+            res = opt.step_accumulated_async([grads] * k_micro, stream, span_events=ev)
         else:
             res = opt.step_async(grads, stream, api=args.api, span_events=ev)
         if res is not None and not res["applied"]:
@@ -337,6 +339,7 @@ def run_ours(args, world, rank, local):
     clocks = ClockSampler(uuid)
     clocks.start()
     launch_ms: list[float] = []
+    last_ms: list[float] = []
     group.barrier()
     torch.cuda.synchronize(dev)
     launches0 = Z.zero_launch_count()
@@ -349,7 +352,9 @@ def run_ours(args, world, rank, local):
     if not opt.last_result(stream)["applied"]:
         raise RuntimeError("benchmark step was skipped: the synthetic gradients overflowed")
     if args.api == "plan":
-        launch_ms = [a.elapsed_time(b) for a, b in spans[:args.steps]]
+        launch_ms = [ev[0].elapsed_time(ev[1]) for ev in spans[:args.steps]]
+        last_ms = ([ev[1].elapsed_time(ev[2]) for ev in spans[:args.steps]]
+                   if k_micro > 1 else [])
     group.barrier()
     launches = Z.zero_launch_count() - launches0
     clock_info = clocks.stop()
@@ -370,14 +375,18 @@ def run_ours(args, world, rank, local):
         # algorithmic bytes of the timed kernel: the whole step's for the fused
         # kernel, the gradient reads for the first pass of the two-pass form
         b_kernel = wl.N * wl.grad_bytes if two_pass else b_alg
+        n_launch = opt.first_pass_launches
         if k_micro > 1:
-            b_kernel = k_micro * wl.N * wl.grad_bytes   # the accumulate passes' gradient reads
+            # the accumulate passes: every micro-batch but the last, whose pass
+            # the third event times apart (it is a pass of the accumulate
+            # kernel too when the step has a second pass)
+            b_kernel = (k_micro - 1) * wl.N * wl.grad_bytes   # their gradient reads
+            n_launch = sum(opt.pass_launches[:-1])
         achieved = b_kernel * wl.psi_pad / (per_step_kernel_ms / 1e3) / 1e9
         # the committed ncu summary covers the fused kernel on the full flat1b_n8
         # workload only
         tpp = (profiled_traffic_per_param()
-               if wl.name == "flat1b_n8" and not two_pass else None)
-        n_launch = opt.first_pass_launches
+               if wl.name == "flat1b_n8" and not two_pass and k_micro == 1 else None)
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4),
                     "traffic": (None if tpp is None else round(tpp * wl.psi_pad / n_launch)),
@@ -391,9 +400,23 @@ def run_ours(args, world, rank, local):
         # a step reads k micro-batches of gradients; the accumulator's round
         # trips are an implementation cost, not algorithmic bytes
         b_alg = k_micro * wl.N * wl.grad_bytes + 26
+        ng = wl.N * wl.grad_bytes
         if roofline:
             roofline["kernel"] = "zero_accum_kernel"
-            roofline["moved_bytes_per_param"] = k_micro * wl.N * wl.grad_bytes + 8 * k_micro - 4
+            # k - 1 accumulate passes: the first writes the accumulator, the
+            # others read and write it
+            roofline["moved_bytes_per_param"] = (k_micro - 1) * ng + 8 * (k_micro - 1) - 4
+            last_step_ms = sum(last_ms) / args.steps
+            # the last micro-batch: fused with the update (reads the
+            # accumulator, 26 B of state), or one more accumulate pass
+            last_moved = ng + 4 + 26 if not two_pass else ng + 8
+            roofline["last_micro_batch"] = {
+                "kernel": "zero_accum_kernel" if two_pass else "zero_fused_kernel (accumulator in)",
+                "ms": round(last_step_ms, 4), "moved_bytes_per_param": last_moved,
+                "moved_gbs": round(last_moved * wl.psi_pad / (last_step_ms / 1e3) / 1e9, 1)}
+            roofline["step_moved_bytes_per_param"] = (
+                k_micro * ng + 8 * (k_micro - 1) + 26 if not two_pass
+                else k_micro * ng + 8 * k_micro - 4 + 30)
     step_gbs = b_alg * wl.psi_pad / (ms / 1e3) / 1e9
 
     e2e = None

@@ -354,8 +354,12 @@ int zero_plan_begin(zero_plan* plan, void* stream);
  * combined gradient, scaled by fp32(1 / (N * k * loss_scale)), to the owner's
  * FP32 accumulator in the workspace, in micro-batch order, from +0.  The
  * overflow check, the norm, the clip and the update use the accumulated
- * gradient.  zero_step and zero_step_into take one batch only and reject
- * k >= 2.
+ * gradient.  When the step needs no second pass (no clip, and no skip of an
+ * in-place step) and the accumulator is the workspace's, the last
+ * micro-batch's buckets add their part to the accumulator and apply the
+ * update in the same pass, leaving the accumulator as the earlier
+ * micro-batches left it; the roundings are the same.  zero_step and
+ * zero_step_into take one batch only and reject k >= 2.
  *
  * First pass over elements [begin, end) of the flat vector.  begin must equal
  * plan->cursor (buckets arrive in flat order, without gaps).  end is a multiple

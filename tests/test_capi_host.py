@@ -255,13 +255,25 @@ def test_accumulation_rules(zero_lib):
     rc = Z.zero_plan_init(plan, [6 * GB, 7 * GB, 8 * GB, 9 * GB], 0, 1 * GB, 2 * GB, 3 * GB, 4 * GB,
                           1 * GB, 2 * GB, 3 * GB, 4 * GB, n, 4, hp, 1.0, 5 * GB,
                           Z.zero_workspace_bytes(n, hp, True))
-    assert rc == Z.ZERO_OK and plan.two_pass == 1
+    # no clip and no in-place skip: the last micro-batch is applied in its own pass
+    assert rc == Z.ZERO_OK and plan.two_pass == 0
     plan.state = 2            # as if begun, without touching a device
     plan.cursor = n
     plan.micro_batch = 0
     assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG
     plan.micro_batch = 1
     assert Z.zero_plan_end(plan, None, 0) == Z.ZERO_ERR_ARG
+    # the update waits for the step-wide decision with clip or an in-place skip
+    for kw, in_place, two in [({"max_grad_norm": 1.0}, False, 1),
+                              ({"skip_on_overflow": True}, True, 1),
+                              ({"skip_on_overflow": True}, False, 0)]:
+        hp2 = Z.make_hparams(micro_batches=3, **kw)
+        dst = [1 * GB, 2 * GB, 3 * GB, 4 * GB] if in_place else [10 * GB, 11 * GB, 12 * GB, 13 * GB]
+        p2 = Z.zero_plan()
+        assert Z.zero_plan_init(p2, [6 * GB, 7 * GB, 8 * GB, 9 * GB], 0, 1 * GB, 2 * GB, 3 * GB,
+                                4 * GB, *dst, n, 4, hp2, 1.0, 5 * GB,
+                                Z.zero_workspace_bytes(n, hp2, in_place)) == Z.ZERO_OK
+        assert p2.two_pass == two, kw
 
 
 @pytest.mark.parametrize("layers", [[5, 9, 3, 9], [100], [], [1000, 1, 1, 999], [38_597_376, 7_082_496]])

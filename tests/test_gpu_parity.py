@@ -297,12 +297,17 @@ def test_async_steps_without_host_reads(zero_lib, oracle_mod):
     (3, 4, "fp32", 0.05, False, False, 262_144, 0.1),
     (2, 2, "fp32", 0.0, True, False, 0, 0.1),
     (4, 5, "bf16", 1.0, True, True, 1_000_000, 0.0),
+    (2, 3, "fp32", 0.0, False, True, 0, 0.1),
+    (5, 2, "fp32", 0.0, True, True, 262_144, 0.0),
 ])
 def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, out_of_place,
                                bucket, wd):
     """k micro-batches reduce-scattered bucket by bucket into the owner's FP32
     accumulator, then one update; against the oracle's accumulation.  With
-    the skip on, micro-batch 1 of step 2 carries a +inf."""
+    the skip on, micro-batch 1 of step 2 carries a +inf.  Without clip, and
+    unless an in-place step may be skipped, the last micro-batch is added and
+    applied in one pass (the first, second, sixth and seventh cases; in the
+    seventh the +inf arrives in that last micro-batch)."""
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     psi = PSI_MULTI_SWEEP if N >= 4 else PSI_SMALL
@@ -441,6 +446,54 @@ def _policy_run(zero_lib, oracle_mod, *, out_of_place, skip, bad_steps, steps, a
     assert res["status"] in (zero_lib.ZERO_OK, zero_lib.ZERO_STEP_SKIPPED)
     assert opt.t == o_t and opt.scaler.scale == o_scale
     compare_state(state_to_numpy(opt.state()), ref, exact=clip == 0.0)
+
+
+@pytest.mark.parametrize("out_of_place", [False, True])
+def test_accumulation_with_device_policy(zero_lib, oracle_mod, out_of_place):
+    """Micro-batch accumulation with t and the dynamic loss scale kept on the
+    device, steps enqueued back to back: step 3 overflows in its last
+    micro-batch and step 4 in its first, and both are skipped.  Out of place
+    the last micro-batch is added and applied in one pass; in place it takes
+    the second pass."""
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    N, k, psi, steps = 4, 3, PSI_SMALL, 6
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(13)) * 0.02
+    opt = ZeroAdam(psi_pad, N, "bf16", skip_on_overflow=True, bucket_elems=131_072,
+                   loss_scale=4096.0, dynamic_loss_scale=True, growth_interval=2,
+                   out_of_place=out_of_place, device=dev, master=master.to(dev),
+                   micro_batches=k, device_policy=True)
+    assert not opt.needs_result
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams()
+    o_t, o_scale, o_good = 0, 4096.0, 0
+    all_micro = []
+    for step in range(1, steps + 1):
+        micro = [_make_grads(N, psi, psi_pad, "bf16", 1e-3 * o_scale, 700 * step + mb)
+                 for mb in range(k)]
+        if step == 3:
+            micro[k - 1][2][999] = float("inf")
+        if step == 4:
+            micro[0][0][5] = float("-inf")
+        all_micro.append(micro)
+        ores = oracle_mod.zero_step_accum([[_np(g) for g in mb] for mb in micro], ref["master"],
+                                          ref["m"], ref["v"], ref["w"], hp, o_t + 1, o_scale,
+                                          True)
+        if ores["applied"]:
+            o_t += 1
+        o_scale, o_good = oracle_mod.loss_scale_update(o_scale, o_good, ores["found_nonfinite"],
+                                                       2, 0.5, 2.0)
+    dev_micro = [[[g.to(dev) for g in mb] for mb in micro] for micro in all_micro]
+    torch.cuda.synchronize()
+    for micro in dev_micro:
+        opt.enqueue_accumulated(micro)
+    res = opt.finish()
+    assert res["status"] == zero_lib.ZERO_OK
+    assert o_t == steps - 2
+    assert opt.t == o_t and opt.scaler.scale == o_scale
+    compare_state(state_to_numpy(opt.state()), ref, exact=True)
 
 
 @pytest.mark.parametrize("out_of_place", [False, True])

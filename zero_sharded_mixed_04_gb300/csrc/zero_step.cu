@@ -279,17 +279,23 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 // One pass: reduce-scatter + scale + check + Adam + BF16 all-gather.  Reads
 // src_*, writes dst_* (the same arrays for an in-place step).
 // One 8-element group: reduce-scatter + scale + check + Adam + BF16 all-gather.
-template <int NT, bool kBF16, int U>
+// kAccIn: the last micro-batch of an accumulated step.  The combined gradient
+// is this micro-batch's scaled contribution added to the FP32 accumulator the
+// earlier micro-batches left in gws (the same two roundings the accumulate
+// kernel makes), and is used at once instead of being written back.
+template <int NT, bool kBF16, bool kAccIn, int U>
 __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s,
                                              const int64_t (&j)[U], unsigned& bad,
                                              double& sumsq) {
     float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
+    float acc[kAccIn ? U : 1][kVec];
     // every load of the U groups is issued before any arithmetic
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         load8(a.src_master, j[u], p[u]);
         load8(a.src_m, j[u], m[u]);
         load8(a.src_v, j[u], v[u]);
+        if constexpr (kAccIn) load8(a.gws, j[u], acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
@@ -298,7 +304,8 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s
         float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-            const float gs = __fmul_rn(g[u][e], s.inv);
+            float gs = __fmul_rn(g[u][e], s.inv);
+            if constexpr (kAccIn) gs = __fadd_rn(acc[u][e], gs);
             bad |= is_nonfinite(gs) ? 1u : 0u;
             sq = fmaf(gs, gs, sq);
             adam_element(gs, p[u][e], m[u][e], v[u][e], s);
@@ -318,7 +325,7 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s
 // src_*, writes dst_* (the same arrays for an in-place step).  Each thread
 // keeps two groups (a grid stride apart) in flight: with 128 registers and two
 // CTAs per SM that measured faster than one group at 64 registers and four.
-template <int NT, bool kBF16>
+template <int NT, bool kBF16, bool kAccIn>
 __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_constant__ StepArgs a) {
     allow_next_launch();
     unsigned bad = 0;
@@ -327,13 +334,20 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
     const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    for (; q + stride < n8; q += 2 * stride) {
+    // FP32 gradients plus the accumulator do not fit two groups in 128
+    // registers without spilling: those take one group at a time.
+    constexpr bool kPairs = kBF16 || !kAccIn;
+    for (; kPairs && q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
-        fused_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 2>(a, s, j, bad, sumsq);
+    }
+    for (; !kPairs && q + stride < n8; q += stride) {
+        const int64_t j[1] = {a.begin + q * kVec};
+        fused_groups<NT, kBF16, kAccIn, 1>(a, s, j, bad, sumsq);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        fused_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 1>(a, s, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -366,39 +380,60 @@ __global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_cons
     finish_cta(a, bad, sumsq);
 }
 
+// U groups of one micro-batch of gradient accumulation: every load first,
+// then the arithmetic, then the stores.
+template <int NT, bool kBF16, int U>
+__device__ __forceinline__ void accum_groups(const StepArgs& a, const Scalars& s,
+                                             const int64_t (&j)[U], unsigned& bad,
+                                             double& sumsq) {
+    float acc[U][kVec], g[U][kVec];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (a.acc_first) {
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) acc[u][e] = 0.0f;
+        } else {
+            load8(a.gws, j[u], acc[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        float sq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            acc[u][e] = __fadd_rn(acc[u][e], __fmul_rn(g[u][e], s.inv));
+            bad |= is_nonfinite(acc[u][e]) ? 1u : 0u;
+            sq = fmaf(acc[u][e], acc[u][e], sq);
+        }
+        if (a.acc_last) sumsq += static_cast<double>(sq);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) store8(a.gws, j[u], acc[u]);
+}
+
 // One micro-batch of gradient accumulation: the reduce-scatter of this
 // micro-batch's contributions, scaled to the batch mean over all N * k of them,
-// added to the owner's FP32 accumulator in the workspace.  The last
-// micro-batch also forms the overflow flag and the norm of the accumulated
-// gradient.
+// added to the owner's FP32 accumulator.  The last micro-batch also forms the
+// overflow flag and the norm of the accumulated gradient.  Two groups per
+// thread are in flight, as in the fused kernel.
 template <int NT, bool kBF16>
-__global__ void __launch_bounds__(kThreads) zero_accum_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) zero_accum_kernel(const __grid_constant__ StepArgs a) {
     allow_next_launch();
     unsigned bad = 0;
     double sumsq = 0.0;
     const Scalars s = step_scalars(a);
     const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < n8;
-         q += stride) {
-        const int64_t j = a.begin + q * kVec;
-        float acc[kVec], g[kVec];
-        if (a.acc_first) {
-#pragma unroll
-            for (int e = 0; e < kVec; ++e) acc[e] = 0.0f;
-        } else {
-            load8(a.gws, j, acc);
-        }
-        combine<NT, kBF16>(a, j, g);
-        float sq = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) {
-            acc[e] = __fadd_rn(acc[e], __fmul_rn(g[e], s.inv));
-            bad |= is_nonfinite(acc[e]) ? 1u : 0u;
-            sq = fmaf(acc[e], acc[e], sq);
-        }
-        if (a.acc_last) sumsq += static_cast<double>(sq);
-        store8(a.gws, j, acc);
+    int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (; q + stride < n8; q += 2 * stride) {
+        const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+        accum_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
+    }
+    if (q < n8) {
+        const int64_t j[1] = {a.begin + q * kVec};
+        accum_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
     }
     finish_cta(a, a.acc_last ? bad : 0u, sumsq);
 }
@@ -547,7 +582,11 @@ using StepKernel = void (*)(StepArgs);
 
 template <int NT, bool B>
 struct FusedK {
-    static constexpr StepKernel fn = zero_fused_kernel<NT, B>;
+    static constexpr StepKernel fn = zero_fused_kernel<NT, B, false>;
+};
+template <int NT, bool B>
+struct FusedAccK {
+    static constexpr StepKernel fn = zero_fused_kernel<NT, B, true>;
 };
 template <int NT, bool B>
 struct ReduceK {
@@ -702,9 +741,10 @@ int32_t micro_batches_of(const zero_adam_hparams* hp) {
     return hp->micro_batches > 1 ? hp->micro_batches : 1;
 }
 
+// The update must wait for the step-wide decision: with clipping, or when a
+// skipped in-place step would have nothing left to restore from.
 bool needs_two_passes(const zero_adam_hparams* hp, bool in_place) {
-    return hp->max_grad_norm > 0.0 || (in_place && hp->skip_on_overflow) ||
-           micro_batches_of(hp) > 1;
+    return hp->max_grad_norm > 0.0 || (in_place && hp->skip_on_overflow);
 }
 
 Scalars make_scalars(const zero_adam_hparams* hp, int32_t N, float loss_scale) {
@@ -727,7 +767,8 @@ Scalars make_scalars(const zero_adam_hparams* hp, int32_t N, float loss_scale) {
 
 size_t workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, bool in_place) {
     size_t b = kGradOffset;
-    if (needs_two_passes(hp, in_place)) b += static_cast<size_t>(psi_pad) * sizeof(float);
+    if (needs_two_passes(hp, in_place) || micro_batches_of(hp) > 1)
+        b += static_cast<size_t>(psi_pad) * sizeof(float);
     return b;
 }
 
@@ -924,7 +965,11 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     const bool bf16 = p->grad_dtype == ZERO_GRAD_BF16;
     const int32_t k = micro_batches_of(&p->hp);
     StepKernel fn;
-    if (k > 1) {
+    if (k > 1 && p->micro_batch == k - 1 && !p->two_pass) {
+        // the last micro-batch of a step with no second pass: accumulate and
+        // update in one pass, without writing the accumulator back
+        fn = pick<FusedAccK>(p->N, bf16);
+    } else if (k > 1) {
         fn = pick<AccumK>(p->N, bf16);
         a.acc_first = p->micro_batch == 0 ? 1 : 0;
         a.acc_last = p->micro_batch == k - 1 ? 1 : 0;

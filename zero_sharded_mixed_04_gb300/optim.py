@@ -197,7 +197,11 @@ class ZeroAdam:
         in ``micro_grads`` (a list of k lists of N gradient buffers; k must equal
         the micro_batches this object was made with).  Each micro-batch's buckets
         are reduce-scattered into the owner's FP32 accumulator in turn; the
-        update follows the last one."""
+        update follows the last one (in the same pass when the step needs no
+        second pass).  ``span_events``: two events recorded around all the
+        micro-batches' launches, or three, the middle one recorded before the
+        last micro-batch's.  ``pass_launches`` then holds the kernel launches of
+        each micro-batch's pass."""
         k = max(1, self.hp.micro_batches)
         if len(micro_grads) != k:
             raise ValueError(f"expected {k} micro-batches, got {len(micro_grads)}")
@@ -217,12 +221,17 @@ class ZeroAdam:
         if span_events is not None:
             span_events[0].record(s)
         n0 = Z.zero_launch_count()
-        for grads in micro_grads:
+        self.pass_launches = []
+        for i, grads in enumerate(micro_grads):
+            if span_events is not None and len(span_events) == 3 and i == k - 1:
+                span_events[1].record(s)
+            n1 = Z.zero_launch_count()
             for b0, b1 in self.bucket_bounds():
                 Z.check(Z.zero_plan_bucket(plan, b0, b1, [g[b0:b1] for g in grads], stream),
                         "zero_plan_bucket")
+            self.pass_launches.append(Z.zero_launch_count() - n1)
         if span_events is not None:
-            span_events[1].record(s)
+            span_events[-1].record(s)
         self.first_pass_launches = Z.zero_launch_count() - n0
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
         self._note_enqueued(s)
@@ -233,6 +242,15 @@ class ZeroAdam:
     def step_accumulated(self, micro_grads, stream=None) -> dict:
         self.enqueue_accumulated(micro_grads, stream)
         return self.finish(stream)
+
+    def step_accumulated_async(self, micro_grads, stream=None, span_events=None) -> dict | None:
+        """step_accumulated without the wait, under the same rule as step_async."""
+        self.enqueue_accumulated(micro_grads, stream, span_events)
+        if self.needs_result:
+            return self.finish(stream)
+        if self.policy_mem is None:
+            self.t += 1
+        return None
 
     # ---------------------------------------------------------------- host gradients
     def make_slots(self, bucket_elems: int | None = None) -> list[list[torch.Tensor]]:
