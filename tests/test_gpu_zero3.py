@@ -7,6 +7,8 @@
   working-weight buffer).  Every layer of the GPT-2-small tensor list is then
   gathered with the two-view prefetch schedule and compared with the oracle's
   step and gather.
+* The same schedule captured as a CUDA graph and replayed twice over
+  different shard contents.
 """
 from __future__ import annotations
 
@@ -82,3 +84,41 @@ def test_two_view_schedule_after_a_step(zero_lib, oracle_mod):
     for i, (b, e) in enumerate(layers):
         want = oracle_mod.gather_range(oshards, b, e)
         assert np.array_equal(got[i].cpu().numpy().view(np.uint16), want), f"layer {i}"
+
+
+def test_two_view_schedule_as_a_cuda_graph(zero_lib, oracle_mod):
+    """The two-view pass captured once and replayed: each replay gathers what
+    the shards hold at that moment, like the eager pass."""
+    from zero_sharded_mixed_04_gb300 import synth
+    from zero_sharded_mixed_04_gb300.optim import Zero3Views
+    dev = torch.device("cuda:0")
+    N = 4
+    sizes = synth.gpt2_small_tensor_sizes()
+    rc, lay, offs = zero_lib.zero_init_layout(sizes, N)
+    assert rc == 0
+    bounds = [0, 1] + [1 + 10 * (i + 1) for i in range(12)] + [len(sizes)]
+    layers = [(offs[bounds[i]], offs[bounds[i + 1] - 1] + sizes[bounds[i + 1] - 1])
+              for i in range(len(bounds) - 1)]
+    S = lay.shard
+    w = torch.empty(lay.psi_pad, dtype=torch.int16, device=dev)
+    shards = [w[r * S:(r + 1) * S] for r in range(N)]
+    outs = [torch.empty(e - b, dtype=torch.int16, device=dev) for b, e in layers]
+
+    def use(i, view):
+        outs[i].copy_(view)
+
+    views = Zero3Views(shards, S, layers, device=dev)
+    graph = views.capture(use)
+    for seed in (41, 42):
+        host = torch.randint(-32768, 32767, (lay.psi_pad,), dtype=torch.int16,
+                             generator=torch.Generator().manual_seed(seed))
+        w.copy_(host)
+        for o in outs:
+            o.fill_(0x5A5A)
+        graph.replay()
+        torch.cuda.synchronize()
+        hs = host.numpy().view(np.uint16)
+        oshards = [hs[r * S:(r + 1) * S] for r in range(N)]
+        for i, (b, e) in enumerate(layers):
+            want = oracle_mod.gather_range(oshards, b, e)
+            assert np.array_equal(outs[i].cpu().numpy().view(np.uint16), want), f"seed {seed} layer {i}"

@@ -1182,9 +1182,19 @@ struct GatherArgs {
 
 constexpr int kGatherUnroll = 4;  // 16-byte vectors in flight per thread
 
+// The gathers are launched as programmatic dependents of whatever precedes
+// them on the stream, so their CTAs are scheduled while that kernel drains.
+// Every thread waits for that kernel to complete before its first access, so
+// the order is the plain stream order for any caller.
+__device__ __forceinline__ void gather_prologue() {
+    allow_next_launch();
+    grid_dependency_wait();
+}
+
 // begin is a multiple of kVec, so every segment is a whole number of 8-element
 // groups on both sides; the last segment may end with n % 8 single elements.
 __global__ void __launch_bounds__(kThreads) zero3_gather_vec_kernel(const __grid_constant__ GatherArgs g) {
+    gather_prologue();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     for (int s = 0; s < g.segments; ++s) {
@@ -1210,6 +1220,7 @@ __global__ void __launch_bounds__(kThreads) zero3_gather_vec_kernel(const __grid
 
 // Any begin: element by element (a layer that starts at an odd offset).
 __global__ void __launch_bounds__(kThreads) zero3_gather_elem_kernel(const __grid_constant__ GatherArgs g) {
+    gather_prologue();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < g.n; i += stride) {
         const int64_t j = g.begin + i;
@@ -1266,11 +1277,19 @@ extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t sh
     int64_t grid = (units + kThreads - 1) / kThreads;
     if (grid > full) grid = full;
     if (grid < 1) grid = 1;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (vec)
-        zero3_gather_vec_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(g);
-    else
-        zero3_gather_elem_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(g);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = vec ? cudaLaunchKernelEx(&cfg, zero3_gather_vec_kernel, g)
+                                : cudaLaunchKernelEx(&cfg, zero3_gather_elem_kernel, g);
+    if (err != cudaSuccess) return ZERO_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
 }

@@ -446,7 +446,11 @@ class Zero3Views:
     def _gather(self, i: int) -> None:
         b, e = self.layers[i]
         slot = i % 2
-        self.side.wait_event(self.released[slot])  # no-op before the first record
+        if i >= 2:
+            # layers 0 and 1 refill views that the previous pass released
+            # before this pass began; the side stream's wait for the caller's
+            # stream at the start of the pass already orders them
+            self.side.wait_event(self.released[slot])
         Z.check(Z.zero3_gather(self.shards, self.N, self.shard, b, e, self.views[slot],
                                self.side), "zero3_gather")
         self.gathered[slot].record(self.side)
@@ -466,3 +470,23 @@ class Zero3Views:
             s.wait_event(self.gathered[slot])
             use(i, self.views[slot][:e - b])
             self.released[slot].record(s)     # the view may be refilled
+
+    def capture(self, use=None):
+        """One pass of run() recorded as a CUDA graph, for a layer list that is
+        the same every pass.  graph.replay() then issues every gather, wait and
+        use(i, view) of the pass with no host work per layer.  The graph holds
+        the shards', views' and layers' addresses, so it reads whatever the
+        shards hold when it is replayed.  use must be capturable: device work
+        only, no host synchronisation.  One eager pass runs first."""
+        fn = use if use is not None else (lambda i, view: None)
+        cur = torch.cuda.current_stream(self.device)
+        cap = torch.cuda.Stream(self.device)
+        cap.wait_stream(cur)
+        with torch.cuda.stream(cap):
+            self.run(fn, cap)           # warm-up: caches the launch shapes
+        cap.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            self.run(fn, cap)
+        cur.wait_stream(cap)
+        return graph
