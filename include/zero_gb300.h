@@ -268,7 +268,41 @@ typedef struct {
                                           previous drains), as zero_step runs them.
                                           The first bucket of each pass over the vector
                                           never overlaps.                                 */
+    int32_t smem_staging;              /* how the one-pass kernel reads its inputs (steps
+                                          without micro-batches, clip or in-place skip):
+                                          ZERO_STAGING_REGISTERS (0, as zero_plan_init
+                                          leaves it) or ZERO_STAGING_TMA.  Set it between
+                                          zero_plan_init and the first zero_plan_bucket.  */
 } zero_plan;
+
+/* Values of zero_plan.smem_staging.
+ *   ZERO_STAGING_REGISTERS  every thread loads its 8-element groups from HBM
+ *                           straight into registers, two groups in flight.
+ *   ZERO_STAGING_TMA        one thread per CTA copies each 1024-element tile
+ *                           (the N gradient chunks and the master/m/v chunks)
+ *                           into one of 2-3 shared-memory stages with TMA bulk
+ *                           copies; four warps compute from shared memory.  The
+ *                           chunk streaming through two or more slots (one in
+ *                           use, the others loading) is the DP-ZeRO blog's
+ *                           two-buffer pattern.  Needs 2 * (N * 1024 * g + 12288)
+ *                           bytes of shared memory per CTA, at most 200 KB
+ *                           (g = 2 for BF16 gradients, 4 for FP32), and the
+ *                           gradients and src master/m/v in device memory (the
+ *                           copies read no pinned host or managed memory);
+ *                           otherwise zero_plan_bucket returns ZERO_ERR_ARG.
+ *                           Every wait in
+ *                           the kernel gives up after about a second: the step
+ *                           then ends with status ZERO_ERR_TIMEOUT and is not
+ *                           applied (out of place, dst is restored from src; in
+ *                           place, the state of the tiles not reached is left
+ *                           as it was and the rest is updated).
+ *   ZERO_STAGING_TMA_TEST_STALL  as ZERO_STAGING_TMA, except that CTA 0 of every
+ *                           launch never copies its first tile, so that waits
+ *                           run out: for testing the timeout path only.
+ * Both forms give the same results bit for bit. */
+#define ZERO_STAGING_REGISTERS 0
+#define ZERO_STAGING_TMA 1
+#define ZERO_STAGING_TMA_TEST_STALL 2
 
 /* Fills *plan from the arguments of zero_step (dst == src) or zero_step_into
  * (dst != src), after the same checks; returns their error codes.  grads is

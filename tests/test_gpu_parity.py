@@ -48,7 +48,8 @@ def _np(t):
 def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, wd=0.0,
                clip=0.0, skip=False, out_of_place=False, bucket=0, loss_scale=1.0,
                dynamic=False, growth_interval=2000, sigma=1e-3, bad_step=0, bad_value=np.inf,
-               seed=1234, api="step", per_bucket_events=False, host_accum=False):
+               seed=1234, api="step", per_bucket_events=False, host_accum=False, staging=0,
+               device_policy=False):
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     unit = N * 128
@@ -61,7 +62,7 @@ def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, 
                    skip_on_overflow=skip, bucket_elems=bucket, loss_scale=loss_scale,
                    dynamic_loss_scale=dynamic, growth_interval=growth_interval,
                    out_of_place=out_of_place, device=dev, master=master.to(dev),
-                   host_grad_accum=host_accum)
+                   host_grad_accum=host_accum, smem_staging=staging, device_policy=device_policy)
     ref = _oracle_state(master.numpy())
     hp = oracle_mod.Hparams(lr=lr, weight_decay=wd, max_grad_norm=clip)
     o_t, o_scale, o_good = 0, loss_scale, 0

@@ -35,6 +35,7 @@
 #include <cstdint>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include <nvtx3/nvToolsExt.h>
@@ -57,6 +58,7 @@ constexpr int kThreads = 256;             // threads per CTA of the streaming ke
 constexpr int kVec = 8;                   // elements per thread per group (16 B of BF16)
 constexpr int kMaxGrid = 2048;            // CTAs per launch, at most
 constexpr int kFinalizeThreads = 1024;
+constexpr int kMaxWarps = 16;             // finish_cta's per-warp slots: blocks of <= 512 threads
 constexpr size_t kCtrlBytes = 256;
 constexpr size_t kPartialsOffset = kCtrlBytes;
 constexpr size_t kGradOffset = kPartialsOffset + kMaxGrid * sizeof(double);  // 256-B aligned
@@ -84,6 +86,7 @@ struct Ctrl {
     float grad_norm;
     zero_step_result result;   // the outcome, when the caller passes no result pointer
     int policy_error;          // device policy: t fell outside the given window
+    unsigned int timeout;      // a bounded wait of the staged kernel gave up
     Scalars scalars;           // device policy: this step's scalars, set by the prologue
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
@@ -112,6 +115,9 @@ struct StepArgs {
     int32_t clip;        // 1: multiply the gradient by ctrl->clip_coef before Adam
     int32_t acc_first;   // accumulation: this is the first micro-batch (start from +0)
     int32_t acc_last;    // accumulation: the last micro-batch (form the step-wide checks)
+    int32_t stages;      // staged kernel: shared-memory stages
+    uint32_t stage_bytes;// staged kernel: bytes of one stage (N gradient chunks + 3 state chunks)
+    int32_t test_stall;  // staged kernel: CTA 0 never copies its first tile (tests the bounded waits)
 };
 
 // The step's scalars: from the kernel arguments, or, under a device policy,
@@ -258,13 +264,13 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->nonfinite, 1u);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, off);
-    __shared__ double warp_sum[kThreads / 32];
+    __shared__ double warp_sum[kMaxWarps];
     if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = sumsq;
     __syncthreads();
     if (threadIdx.x == 0) {
         double t = 0.0;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) t += warp_sum[w];
+        const int warps = static_cast<int>(blockDim.x >> 5);  // whole warps only
+        for (int w = 0; w < warps; ++w) t += warp_sum[w];
         // A bucket launch may start while the previous one drains (programmatic
         // dependent launch).  Its slot update must still come after the
         // previous launch's: wait for that grid to complete first.  Without a
@@ -276,8 +282,6 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 
 // ------------------------------------------------------------------ kernels
 
-// One pass: reduce-scatter + scale + check + Adam + BF16 all-gather.  Reads
-// src_*, writes dst_* (the same arrays for an in-place step).
 // One 8-element group: reduce-scatter + scale + check + Adam + BF16 all-gather.
 // kAccIn: the last micro-batch of an accumulated step.  The combined gradient
 // is this micro-batch's scaled contribution added to the FP32 accumulator the
@@ -349,6 +353,232 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
         const int64_t j[1] = {a.begin + q * kVec};
         fused_groups<NT, kBF16, kAccIn, 1>(a, s, j, bad, sumsq);
     }
+    finish_cta(a, bad, sumsq);
+}
+
+// ------------------------------------------------------------------ staged one-pass kernel
+//
+// The same one-pass step with each tile of kTile elements staged in shared
+// memory.  One producer thread copies a tile's N gradient chunks and its
+// master/m/v chunks from HBM into a stage with TMA bulk copies
+// (cp.async.bulk), counted in the stage's "full" mbarrier.  Four consumer
+// warps wait on it, compute from shared memory, store the results straight to
+// HBM and arrive on the stage's "empty" mbarrier, which the producer waits on
+// before it refills the stage.  With 2-3 stages per CTA, two tiles are in
+// flight while one is computed: the two-slot buffer (one in use, one loading)
+// of the offload pattern, inside a kernel.
+//
+// Every wait is bounded by the global timer.  A wait that gives up sets
+// ctrl->timeout; the producer then waits (again bounded) for the copies it
+// issued, so that no copy is still landing in shared memory when the CTA
+// exits, and the step ends with ZERO_ERR_TIMEOUT.
+//
+// Consumer thread c owns elements [4c, 4c + 4) and [512 + 4c, 512 + 4c + 4)
+// of a tile, so each shared-memory load of a warp covers consecutive 8- or
+// 16-byte words (no bank conflicts) and each global store of a warp is one
+// contiguous run.  The element arithmetic is the register kernel's.
+
+constexpr int kTile = 1024;
+constexpr int kStagedConsumerWarps = 4;
+constexpr int kStagedThreads = 32 * (kStagedConsumerWarps + 1);  // + the producer warp
+constexpr int kHalfTile = kTile / 2;
+static_assert(kHalfTile == 32 * kStagedConsumerWarps * 4, "two 4-element chunks per consumer");
+constexpr int kMaxStages = 3;
+constexpr size_t kStagedSmemLimit = 200 * 1024;  // dynamic shared memory per CTA, at most
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Waits for the completion of the barrier's phase of the given parity; false
+// if it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+// A TMA bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+// Shared-memory loads, by shared-window address.  The memory clobber keeps
+// them after the mbarrier wait that makes the stage's bytes visible.
+__device__ __forceinline__ uint2 lds_u2(const void* p) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "r"(smem_addr(p))
+                 : "memory");
+    return r;
+}
+__device__ __forceinline__ float4 lds_f4(const void* p) {
+    float4 r;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "r"(smem_addr(p))
+                 : "memory");
+    return r;
+}
+
+// Consumer work on 4 elements: the tile-relative element e (a multiple of 4)
+// of the stage st, flat index j.
+template <int NT, bool kBF16>
+__device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s,
+                                             const unsigned char* st, int e, int64_t j,
+                                             unsigned& bad, double& sumsq) {
+    constexpr uint32_t gbytes = kBF16 ? 2 : 4;
+    const int n = NT > 0 ? NT : a.N;
+    float g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // rank order from +0, as in the register kernel
+#pragma unroll(NT > 0 ? NT : 1)
+    for (int i = 0; i < n; ++i) {
+        const unsigned char* chunk = st + static_cast<size_t>(i) * kTile * gbytes;
+        if constexpr (kBF16) {
+            const uint2 r = lds_u2(chunk + e * 2);
+            g[0] = __fadd_rn(g[0], bf16_lo(r.x));
+            g[1] = __fadd_rn(g[1], bf16_hi(r.x));
+            g[2] = __fadd_rn(g[2], bf16_lo(r.y));
+            g[3] = __fadd_rn(g[3], bf16_hi(r.y));
+        } else {
+            const float4 r = lds_f4(chunk + e * 4);
+            g[0] = __fadd_rn(g[0], r.x);
+            g[1] = __fadd_rn(g[1], r.y);
+            g[2] = __fadd_rn(g[2], r.z);
+            g[3] = __fadd_rn(g[3], r.w);
+        }
+    }
+    const unsigned char* state = st + static_cast<size_t>(n) * kTile * gbytes;
+    const float4 P = lds_f4(state + e * 4);
+    const float4 M = lds_f4(state + (kTile + e) * 4);
+    const float4 V = lds_f4(state + (2 * kTile + e) * 4);
+    float p[4] = {P.x, P.y, P.z, P.w}, m[4] = {M.x, M.y, M.z, M.w}, v[4] = {V.x, V.y, V.z, V.w};
+    float sq = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float gs = __fmul_rn(g[q], s.inv);
+        bad |= is_nonfinite(gs) ? 1u : 0u;
+        sq = fmaf(gs, gs, sq);
+        adam_element(gs, p[q], m[q], v[q], s);
+    }
+    sumsq += static_cast<double>(sq);
+    __stcs(reinterpret_cast<float4*>(a.dst_master + j), make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(reinterpret_cast<float4*>(a.dst_m + j), make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(reinterpret_cast<float4*>(a.dst_v + j), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<uint2*>(a.dst_w + j),
+           make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
+}
+
+template <int NT, bool kBF16>
+__global__ void __launch_bounds__(kStagedThreads)
+    zero_fused_staged_kernel(const __grid_constant__ StepArgs a) {
+    allow_next_launch();
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr uint32_t gbytes = kBF16 ? 2 : 4;
+    const int n_ranks = NT > 0 ? NT : a.N;
+    const int stages = a.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(stages) * a.stage_bytes);
+    uint64_t* empty = full + stages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < stages; ++k) {
+            mbar_init(&full[k], 1);                      // the producer's arrive + the bytes
+            mbar_init(&empty[k], kStagedConsumerWarps);  // one arrive per consumer warp
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const Scalars s = step_scalars(a);
+    const int64_t range = (policy_off(a) ? 0 : a.n8) * kVec;  // a multiple of 8
+    const int64_t ntiles = (range + kTile - 1) / kTile;
+    unsigned bad = 0, timed_out = 0;
+    double sumsq = 0.0;
+    if (warp == kStagedConsumerWarps) {
+        if (lane == 0) {  // the producer
+            int64_t k = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++k) {
+                const int st_i = static_cast<int>(k % stages);
+                if (k >= stages &&
+                    !mbar_wait(&empty[st_i], static_cast<uint32_t>((k / stages - 1) & 1))) {
+                    timed_out = 1;
+                    break;
+                }
+                if (a.test_stall && blockIdx.x == 0 && k == 0) continue;  // never copied
+                const int64_t e0 = t * kTile;
+                const int64_t len = (range - e0 < kTile) ? range - e0 : kTile;
+                const int64_t j = a.begin + e0;
+                unsigned char* st = smem + static_cast<size_t>(st_i) * a.stage_bytes;
+                const uint32_t gb = static_cast<uint32_t>(len) * gbytes;
+                const uint32_t sb = static_cast<uint32_t>(len) * 4u;
+                mbar_arrive_expect_tx(&full[st_i], static_cast<uint32_t>(n_ranks) * gb + 3u * sb);
+                for (int i = 0; i < n_ranks; ++i)
+                    bulk_load(st + static_cast<size_t>(i) * kTile * gbytes,
+                              static_cast<const unsigned char*>(a.grads[i]) + (j - a.gbase) * gbytes,
+                              gb, &full[st_i]);
+                unsigned char* state = st + static_cast<size_t>(n_ranks) * kTile * gbytes;
+                bulk_load(state, a.src_master + j, sb, &full[st_i]);
+                bulk_load(state + kTile * 4, a.src_m + j, sb, &full[st_i]);
+                bulk_load(state + 2 * kTile * 4, a.src_v + j, sb, &full[st_i]);
+            }
+            if (timed_out) {
+                // let every copy already issued land before the CTA may exit
+                for (int64_t kk = (k > stages ? k - stages : 0); kk < k; ++kk)
+                    mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
+            }
+        }
+    } else {  // the consumers
+        const int c = threadIdx.x;  // 0 .. 127
+        int64_t k = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++k) {
+            const int st_i = static_cast<int>(k % stages);
+            if (!mbar_wait(&full[st_i], static_cast<uint32_t>((k / stages) & 1))) {
+                timed_out = 1;
+                break;
+            }
+            const int64_t e0 = t * kTile;
+            const int64_t len = (range - e0 < kTile) ? range - e0 : kTile;
+            const unsigned char* st = smem + static_cast<size_t>(st_i) * a.stage_bytes;
+            const int e_a = 4 * c, e_b = kHalfTile + 4 * c;
+            if (e_a < len) staged_chunk<NT, kBF16>(a, s, st, e_a, a.begin + e0 + e_a, bad, sumsq);
+            if (e_b < len) staged_chunk<NT, kBF16>(a, s, st, e_b, a.begin + e0 + e_b, bad, sumsq);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st_i]);
+        }
+    }
+    if (timed_out) atomicOr(&a.ctrl->timeout, 1u);
     finish_cta(a, bad, sumsq);
 }
 
@@ -515,7 +745,8 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         const double norm = sqrt(sumsq);
         const int nonfinite = ctrl->nonfinite != 0u;
         const int window_miss = (policy != nullptr && ctrl->policy_error) ? 1 : 0;
-        const int skip = ((skip_on_overflow && nonfinite) || window_miss) ? 1 : 0;
+        const int timeout = ctrl->timeout != 0u;
+        const int skip = ((skip_on_overflow && nonfinite) || window_miss || timeout) ? 1 : 0;
         float coef = 1.0f;
         if (max_norm > 0.0 && !skip) {
             const double c = max_norm / (norm + 1e-6);
@@ -525,7 +756,10 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         ctrl->clip_coef = coef;
         ctrl->grad_norm = static_cast<float>(norm);
         zero_step_result r;
-        r.status = window_miss ? ZERO_ERR_POLICY_WINDOW : (skip ? ZERO_STEP_SKIPPED : ZERO_OK);
+        r.status = timeout       ? ZERO_ERR_TIMEOUT
+                   : window_miss ? ZERO_ERR_POLICY_WINDOW
+                   : skip        ? ZERO_STEP_SKIPPED
+                                 : ZERO_OK;
         r.found_nonfinite = static_cast<uint32_t>(nonfinite);
         r.grad_norm = static_cast<float>(norm);
         r.clip_coef = coef;
@@ -534,7 +768,7 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
             // the host-side rule, kept on the device: t counts applied steps;
             // the dynamic scale backs off after an overflow, grows after
             // growth_interval clean steps
-            if (!window_miss) {
+            if (!window_miss && !timeout) {
                 if (!skip) policy->t += 1;
                 if (policy->growth_interval > 0) {
                     if (nonfinite) {
@@ -594,6 +828,10 @@ struct ReduceK {
 };
 
 template <int NT, bool B>
+struct StagedK {
+    static constexpr StepKernel fn = zero_fused_staged_kernel<NT, B>;
+};
+template <int NT, bool B>
 struct AccumK {
     static constexpr StepKernel fn = zero_accum_kernel<NT, B>;
 };
@@ -609,16 +847,17 @@ StepKernel pick(int N, bool bf16) {
     }
 }
 
-// CTAs per SM for a kernel on a device, measured once and cached.
-int resident_ctas(const void* fn, int device, int threads) {
+// CTAs per SM for a kernel on a device with the given dynamic shared memory,
+// measured once and cached.
+int resident_ctas(const void* fn, int device, int threads, size_t smem = 0) {
     static std::mutex mu;
-    static std::map<std::pair<const void*, int>, int> cache;
+    static std::map<std::tuple<const void*, int, size_t>, int> cache;
     std::lock_guard<std::mutex> lock(mu);
-    auto key = std::make_pair(fn, device);
+    auto key = std::make_tuple(fn, device, smem);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1)
         n = 1;
     cache[key] = n;
     return n;
@@ -637,11 +876,21 @@ int sm_count(int device) {
     return n;
 }
 
+// Launch shape of a step kernel: the register kernels take one 8-element group
+// per thread and no dynamic shared memory; the staged kernel one kTile tile
+// per CTA and `smem` bytes of stages.
+struct Shape {
+    int threads = kThreads;
+    size_t smem = 0;
+    bool tiles = false;
+};
+
 // Persistent grid: as many CTAs as fit on the device at once (a multiple of
 // the SM count), fewer if the range is small.
-int grid_for(const void* fn, int device, int64_t n8) {
-    const int64_t full = static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, kThreads);
-    const int64_t need = (n8 + kThreads - 1) / kThreads;
+int grid_for(const void* fn, int device, int64_t n8, const Shape& sh = Shape{}) {
+    const int64_t full =
+        static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, sh.threads, sh.smem);
+    const int64_t need = sh.tiles ? (n8 * kVec + kTile - 1) / kTile : (n8 + sh.threads - 1) / sh.threads;
     int64_t g = need < full ? need : full;
     if (g > kMaxGrid) g = kMaxGrid;
     return g < 1 ? 1 : static_cast<int>(g);
@@ -652,19 +901,19 @@ int grid_for(const void* fn, int device, int64_t n8) {
 // launch); only first-pass bucket launches of one step, whose elements are
 // disjoint from the previous bucket's, ask for it.
 bool launch(StepKernel fn, int device, const StepArgs& a, cudaStream_t stream,
-            bool overlap_previous = false) {
-    const int grid = grid_for(reinterpret_cast<const void*>(fn), device, a.n8);
-    if (overlap_previous) {
+            bool overlap_previous = false, const Shape& sh = Shape{}) {
+    const int grid = grid_for(reinterpret_cast<const void*>(fn), device, a.n8, sh);
+    if (overlap_previous || sh.smem > 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = 0;
+        cfg.blockDim = dim3(static_cast<unsigned>(sh.threads));
+        cfg.dynamicSmemBytes = sh.smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = overlap_previous ? 1 : 0;
         if (cudaLaunchKernelEx(&cfg, fn, a) != cudaSuccess) return false;
     } else {
         fn<<<grid, kThreads, 0, stream>>>(a);
@@ -688,7 +937,7 @@ constexpr int64_t kLaunchAlignGroups = 32;  // 256 elements
 // kernel before it on the stream only if overlap_first; the others always
 // follow a sub-launch of the same range.
 bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t end,
-                  cudaStream_t stream, bool overlap_first) {
+                  cudaStream_t stream, bool overlap_first, const Shape& sh = Shape{}) {
     const int64_t groups = (end - begin) / kVec;
     if (groups <= 0) return true;
     const int64_t parts = (groups * kVec + kLaunchElems - 1) / kLaunchElems;
@@ -702,12 +951,52 @@ bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t 
     for (int64_t k = 0, g0 = 0; g0 < groups; ++k, g0 += per) {
         a.begin = begin + g0 * kVec;
         a.n8 = (groups - g0 < per) ? groups - g0 : per;
-        if (!launch(fn, device, a, stream, k > 0 || overlap_first)) return false;
+        if (!launch(fn, device, a, stream, k > 0 || overlap_first, sh)) return false;
     }
     return true;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The staged kernel's TMA copies read device memory only (not pinned host or
+// managed memory, which the register kernels can also read).
+bool device_memory(const void* ptr) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the error that query may leave behind
+        return false;
+    }
+    return attr.type == cudaMemoryTypeDevice;
+}
+
+// Stages of the staged kernel for N ranks: as many as fit (at most
+// kMaxStages) in kStagedSmemLimit, at least two.  Fills a.stages,
+// a.stage_bytes and the launch shape; false if two stages do not fit.
+bool staged_shape(StepKernel fn, int device, int N, bool bf16, StepArgs& a, Shape& sh) {
+    const size_t stage = static_cast<size_t>(N) * kTile * (bf16 ? 2 : 4) + 3 * size_t(kTile) * 4;
+    int stages = kMaxStages;
+    while (stages >= 2 && stages * (stage + 16) > kStagedSmemLimit) --stages;
+    if (stages < 2) return false;
+    {
+        static std::mutex mu;
+        static std::map<std::pair<const void*, int>, bool> opted_in;
+        std::lock_guard<std::mutex> lock(mu);
+        auto key = std::make_pair(reinterpret_cast<const void*>(fn), device);
+        if (!opted_in[key]) {
+            if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kStagedSmemLimit)) != cudaSuccess)
+                return false;
+            opted_in[key] = true;
+        }
+    }
+    a.stages = stages;
+    a.stage_bytes = static_cast<uint32_t>(stage);
+    sh.threads = kStagedThreads;
+    sh.smem = stages * stage + 2 * stages * sizeof(uint64_t);
+    sh.tiles = true;
+    return true;
+}
 
 struct Span {
     uintptr_t lo, hi;
@@ -964,8 +1253,20 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
     const bool bf16 = p->grad_dtype == ZERO_GRAD_BF16;
     const int32_t k = micro_batches_of(&p->hp);
+    if (p->smem_staging < ZERO_STAGING_REGISTERS || p->smem_staging > ZERO_STAGING_TMA_TEST_STALL)
+        return ZERO_ERR_ARG;
     StepKernel fn;
-    if (k > 1 && p->micro_batch == k - 1 && !p->two_pass) {
+    Shape shape;
+    if (k == 1 && !p->two_pass && p->smem_staging != ZERO_STAGING_REGISTERS) {
+        fn = pick<StagedK>(p->N, bf16);
+        if (!staged_shape(fn, device, p->N, bf16, a, shape)) return ZERO_ERR_ARG;
+        for (int i = 0; i < p->N; ++i)
+            if (!device_memory(a.grads[i])) return ZERO_ERR_ARG;
+        if (begin == 0 &&
+            (!device_memory(p->src_master) || !device_memory(p->src_m) || !device_memory(p->src_v)))
+            return ZERO_ERR_ARG;
+        a.test_stall = p->smem_staging == ZERO_STAGING_TMA_TEST_STALL ? 1 : 0;
+    } else if (k > 1 && p->micro_batch == k - 1 && !p->two_pass) {
         // the last micro-batch of a step with no second pass: accumulate and
         // update in one pass, without writing the accumulator back
         fn = pick<FusedAccK>(p->N, bf16);
@@ -983,7 +1284,7 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     // 0.  The first bucket of a pass (begin == 0) never overlaps: when
     // accumulating it reads what the previous micro-batch wrote.
     const bool overlap = p->overlap_buckets != 0 && begin > 0;
-    if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap))
+    if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap, shape))
         return ZERO_ERR_CUDA;
     p->cursor = end;
     // accumulating: a micro-batch that covered the vector hands over to the
@@ -1027,7 +1328,10 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
         // the first update launch waits for the finalize kernel in stream order
         if (!launch_range(zero_update_kernel, device, a, 0, p->psi_pad, stream, false))
             return ZERO_ERR_CUDA;
-    } else if (!p->in_place && (p->hp.skip_on_overflow || p->policy != nullptr)) {
+    } else if (!p->in_place && (p->hp.skip_on_overflow || p->policy != nullptr ||
+                                p->smem_staging != ZERO_STAGING_REGISTERS)) {
+        // a skipped step (overflow, a t outside the policy's window, a timed-out
+        // staged wait) must leave dst equal to src
         a.begin = 0;
         a.n8 = p->psi_pad / kVec;
         if (!launch(zero_restore_kernel, device, a, stream)) return ZERO_ERR_CUDA;

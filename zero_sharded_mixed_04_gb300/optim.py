@@ -62,7 +62,8 @@ class ZeroAdam:
                  skip_on_overflow=False, bucket_elems=0, loss_scale=1.0,
                  dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
                  device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0,
-                 host_grad_accum: bool = False, device_policy: bool = False):
+                 host_grad_accum: bool = False, device_policy: bool = False,
+                 smem_staging: int = 0):
         self.psi_pad, self.N = psi_pad, N
         self.grad_dtype = Z.ZERO_GRAD_BF16 if grad_dtype == "bf16" else Z.ZERO_GRAD_FP32
         self.hp = Z.make_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1,
@@ -70,6 +71,9 @@ class ZeroAdam:
         self.t = 0  # applied steps so far
         self.scaler = LossScaler(loss_scale, dynamic_loss_scale, growth_interval)
         self.out_of_place = out_of_place
+        # smem_staging: zero_plan.smem_staging for the plan-path steps
+        # (ZERO_STAGING_TMA stages every tile in shared memory by TMA bulk copies)
+        self.smem_staging = smem_staging
         self.device = torch.device(device)
         sets = 2 if out_of_place else 1
         self._bufs = []
@@ -137,7 +141,8 @@ class ZeroAdam:
             keep them from overlapping."""
         self.hp.step = self.t + 1
         src = self._bufs[self.cur]
-        if api == "plan" or self.grad_accum is not None or self.policy_mem is not None:
+        if (api == "plan" or self.grad_accum is not None or self.policy_mem is not None
+                or self.smem_staging):
             return self._enqueue_plan(grads, src, stream, bucket_events, span_events)
         if self.out_of_place:
             dst = self._bufs[1 - self.cur]
@@ -169,6 +174,7 @@ class ZeroAdam:
         # nothing but bucket launches goes between the buckets unless events
         # are recorded around each one
         plan.overlap_buckets = 0 if bucket_events is not None else 1
+        plan.smem_staging = self.smem_staging
         self._apply_policy(plan, stream)
         Z.check(Z.zero_plan_begin(plan, stream), "zero_plan_begin")
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -276,6 +282,7 @@ class ZeroAdam:
                                     dst["v"], dst["w"], self.psi_pad, self.N, self.hp,
                                     self.scaler.scale, self.workspace, self.ws_bytes,
                                     self.grad_accum), "zero_plan_init")
+        plan.smem_staging = self.smem_staging
         self._apply_policy(plan, s)
         Z.check(Z.zero_plan_begin(plan, s), "zero_plan_begin")
         if not hasattr(self, "_slot_events"):

@@ -49,6 +49,10 @@ ZERO_NOALLOC_SCRATCH_BYTES = 16640 + 4 * ZERO_NOALLOC_MAX_TWO_PASS_ELEMS
 ZERO_GRAD_BF16 = 0
 ZERO_GRAD_FP32 = 1
 
+ZERO_STAGING_REGISTERS = 0
+ZERO_STAGING_TMA = 1
+ZERO_STAGING_TMA_TEST_STALL = 2
+
 
 class zero_layout(ctypes.Structure):
     _fields_ = [("psi", ctypes.c_int64), ("psi_pad", ctypes.c_int64), ("shard", ctypes.c_int64),
@@ -81,7 +85,8 @@ class zero_plan(ctypes.Structure):
                 ("N", ctypes.c_int32), ("in_place", ctypes.c_int32), ("two_pass", ctypes.c_int32),
                 ("state", ctypes.c_int32), ("micro_batch", ctypes.c_int32),
                 ("policy_t_count", ctypes.c_int32), ("policy_t_first", ctypes.c_int64),
-                ("policy", ctypes.c_void_p), ("overlap_buckets", ctypes.c_int32)]
+                ("policy", ctypes.c_void_p), ("overlap_buckets", ctypes.c_int32),
+                ("smem_staging", ctypes.c_int32)]
 
 
 class zero_device_policy(ctypes.Structure):
