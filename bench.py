@@ -2,6 +2,7 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload flat1b_n8] [--api plan|step] [--in-place]
+                [--staging tma|registers]
 
 One step is one pass of the whole hot path over one batch of synthetic
 gradients, resident in device memory when the timed region starts:
@@ -13,8 +14,10 @@ gradients, resident in device memory when the timed region starts:
   - the host bookkeeping (step counter, dynamic loss scale).
 The default workload is flat1b_n8: 1,000,000,000 parameters, N=8 BF16 ranks,
 25,000,000-element buckets, dynamic loss scale from 65536, skip on overflow.
-It runs out of place (zero_step_into), so the skip decision needs no second
-pass.
+It runs out of place (the plan entry points, as zero_step_into), so the skip
+decision needs no second pass.  The one-pass kernel stages every 2048-element
+tile in shared memory with TMA bulk copies (ZERO_STAGING_TMA); --staging
+registers times the kernel that loads straight into registers instead.
 
 The printed JSON line carries:
   - value: params/s over all GPUs;
@@ -51,7 +54,12 @@ METRIC = "params/sec and achieved HBM GB/s (fraction of GB300 peak) per fused Ze
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_04_gb300", "csrc", "zero_step.cu")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "zero_fused_kernel_flat1b_n8.md")
+# the committed ncu summary of each one-pass kernel on the full flat1b_n8 workload
+PROFILE_SUMMARY = {
+    "zero_fused_kernel": os.path.join(ROOT, "profiles", "zero_fused_kernel_flat1b_n8.md"),
+    "zero_fused_staged_kernel": os.path.join(ROOT, "profiles",
+                                             "zero_fused_staged_kernel_flat1b_n8.md"),
+}
 
 
 def parse_args(argv=None):
@@ -75,7 +83,7 @@ def parse_args(argv=None):
     ap.add_argument("--host-grad-accum", action="store_true",
                     help="keep the owner's FP32 gradient shard in pinned host memory "
                          "(reached over the host link); forces the two-pass form")
-    ap.add_argument("--staging", choices=["registers", "tma"], default="registers",
+    ap.add_argument("--staging", choices=["registers", "tma"], default="tma",
                     help="how the one-pass kernel reads its inputs: straight into registers, or "
                          "tile by tile into shared-memory stages by TMA bulk copies")
     ap.add_argument("--micro-batches", type=int, default=0,
@@ -224,11 +232,11 @@ def kernel_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic_per_param() -> float | None:
-    """DRAM bytes per parameter of the fused kernel from the committed ncu
+def profiled_traffic_per_param(kernel: str) -> float | None:
+    """DRAM bytes per parameter of a one-pass kernel from its committed ncu
     summary, if it was taken on the kernel source as it is now."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY[kernel]).read()
     except OSError:
         return None
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
@@ -390,9 +398,9 @@ def run_ours(args, world, rank, local):
         # the committed ncu summary covers the fused kernel on the full flat1b_n8
         # workload only
         staged = args.staging == "tma" and not two_pass and k_micro == 1
-        tpp = (profiled_traffic_per_param()
-               if wl.name == "flat1b_n8" and not two_pass and k_micro == 1 and not staged
-               else None)
+        tpp = (profiled_traffic_per_param("zero_fused_staged_kernel" if staged
+                                          else "zero_fused_kernel")
+               if wl.name == "flat1b_n8" and not two_pass and k_micro == 1 else None)
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4),
                     "traffic": (None if tpp is None else round(tpp * wl.psi_pad / n_launch)),

@@ -278,15 +278,15 @@ typedef struct {
 /* Values of zero_plan.smem_staging.
  *   ZERO_STAGING_REGISTERS  every thread loads its 8-element groups from HBM
  *                           straight into registers, two groups in flight.
- *   ZERO_STAGING_TMA        one thread per CTA copies each 1024-element tile
+ *   ZERO_STAGING_TMA        one thread per CTA copies each 2048-element tile
  *                           (the N gradient chunks and the master/m/v chunks)
- *                           into one of 2-3 shared-memory stages with TMA bulk
- *                           copies; four warps compute from shared memory.  The
- *                           chunk streaming through two or more slots (one in
- *                           use, the others loading) is the DP-ZeRO blog's
- *                           two-buffer pattern.  Needs 2 * (N * 1024 * g + 12288)
- *                           bytes of shared memory per CTA, at most 200 KB
- *                           (g = 2 for BF16 gradients, 4 for FP32), and the
+ *                           into one of two shared-memory stages with TMA bulk
+ *                           copies; sixteen warps compute from shared memory.
+ *                           The chunks streaming through two slots (one in use,
+ *                           one loading) is the DP-ZeRO blog's two-buffer
+ *                           pattern.  Needs 2 * (N * 2048 * g + 24576) bytes of
+ *                           shared memory per CTA, at most 200 KB (g = 2 for
+ *                           BF16 gradients, 4 for FP32: N <= 18 and N <= 9), and the
  *                           gradients and src master/m/v in device memory (the
  *                           copies read no pinned host or managed memory);
  *                           otherwise zero_plan_bucket returns ZERO_ERR_ARG.

@@ -99,17 +99,18 @@ def _plan_step(Z, grads, src, dst, n, N, hp, staging, res):
     return int(res[0])
 
 
-@pytest.mark.parametrize("tiles", [32, 1024])
-def test_staged_wait_runs_out(zero_lib, tiles):
+@pytest.mark.parametrize("n", [32_768, 4_194_304])
+def test_staged_wait_runs_out(zero_lib, n):
     """CTA 0 never copies its first tile (ZERO_STAGING_TMA_TEST_STALL), so its
-    consumers' wait runs out after about a second.  With more tiles than
-    stages, the producer's wait for a free stage runs out too, and it then
+    consumers' wait runs out after about a second.  With more tiles per CTA
+    than stages (the larger case: 2048 tiles of 2048 elements over at most 304
+    CTAs), the producer's wait for a free stage runs out too, and it then
     waits for the copies it issued.  The step ends with ZERO_ERR_TIMEOUT and,
     out of place, leaves dst equal to src.  The context stays usable: the next
     step, staged, equals the register kernel's bit for bit."""
     Z = zero_lib
     dev = torch.device("cuda:0")
-    N, n = 4, 1024 * tiles
+    N = 4
     grads = [(torch.randn(n, generator=torch.Generator().manual_seed(60 + i)) * 1e-3).to(
         torch.bfloat16).to(dev) for i in range(N)]
     src = [torch.randn(n, device=dev) * 0.02, torch.rand(n, device=dev) * 1e-4,
@@ -135,8 +136,8 @@ def test_staged_wait_runs_out(zero_lib, tiles):
 
 
 def test_staged_rejects_stages_that_do_not_fit(zero_lib):
-    """N = 64 FP32 gradients need 268 KB per stage: the plan refuses before
-    launching anything."""
+    """Two stages for N = 64 FP32 gradients would need 1.1 MB: the plan
+    refuses before launching anything."""
     Z = zero_lib
     dev = torch.device("cuda:0")
     N, n = 64, 64 * 128

@@ -58,7 +58,7 @@ constexpr int kThreads = 256;             // threads per CTA of the streaming ke
 constexpr int kVec = 8;                   // elements per thread per group (16 B of BF16)
 constexpr int kMaxGrid = 2048;            // CTAs per launch, at most
 constexpr int kFinalizeThreads = 1024;
-constexpr int kMaxWarps = 16;             // finish_cta's per-warp slots: blocks of <= 512 threads
+constexpr int kMaxWarps = 32;             // finish_cta's per-warp slots: blocks of <= 1024 threads
 constexpr size_t kCtrlBytes = 256;
 constexpr size_t kPartialsOffset = kCtrlBytes;
 constexpr size_t kGradOffset = kPartialsOffset + kMaxGrid * sizeof(double);  // 256-B aligned
@@ -361,29 +361,38 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
 // The same one-pass step with each tile of kTile elements staged in shared
 // memory.  One producer thread copies a tile's N gradient chunks and its
 // master/m/v chunks from HBM into a stage with TMA bulk copies
-// (cp.async.bulk), counted in the stage's "full" mbarrier.  Four consumer
+// (cp.async.bulk), counted in the stage's "full" mbarrier.  Sixteen consumer
 // warps wait on it, compute from shared memory, store the results straight to
 // HBM and arrive on the stage's "empty" mbarrier, which the producer waits on
-// before it refills the stage.  With 2-3 stages per CTA, two tiles are in
-// flight while one is computed: the two-slot buffer (one in use, one loading)
-// of the offload pattern, inside a kernel.
+// before it refills the stage.  Two stages per CTA: one tile is computed while
+// the next loads, the two-slot buffer (one in use, one loading) of the offload
+// pattern, inside a kernel.
+//
+// Measured on Psi = 1e9, N = 8 BF16 (interleaved runs on one GPU, against the
+// register kernel at 5.94 ms per step): 2048-element tiles, 16 consumer warps
+// and 2 stages gave 5.89 ms; 8 warps 5.90; 1024-element tiles with 8 warps
+// 5.91, with 4 warps 6.03; 3 stages of 1024 with 4 warps 6.21; 4 and 6 stages
+// were slower still.  More consumer warps per SM mattered, deeper staging did
+// not.
 //
 // Every wait is bounded by the global timer.  A wait that gives up sets
 // ctrl->timeout; the producer then waits (again bounded) for the copies it
 // issued, so that no copy is still landing in shared memory when the CTA
 // exits, and the step ends with ZERO_ERR_TIMEOUT.
 //
-// Consumer thread c owns elements [4c, 4c + 4) and [512 + 4c, 512 + 4c + 4)
-// of a tile, so each shared-memory load of a warp covers consecutive 8- or
-// 16-byte words (no bank conflicts) and each global store of a warp is one
-// contiguous run.  The element arithmetic is the register kernel's.
+// Consumer thread c owns the 4-element chunks starting at 4c, 4c + 4C,
+// 4c + 8C, ... of a tile (C consumer threads), so each shared-memory load of a
+// warp covers consecutive 8- or 16-byte words (no bank conflicts) and each
+// global store of a warp is one contiguous run.  The element arithmetic is
+// the register kernel's.
 
-constexpr int kTile = 1024;
-constexpr int kStagedConsumerWarps = 4;
-constexpr int kStagedThreads = 32 * (kStagedConsumerWarps + 1);  // + the producer warp
-constexpr int kHalfTile = kTile / 2;
-static_assert(kHalfTile == 32 * kStagedConsumerWarps * 4, "two 4-element chunks per consumer");
-constexpr int kMaxStages = 3;
+constexpr int kTile = 2048;
+constexpr int kStagedConsumerWarps = 16;
+constexpr int kStagedConsumers = 32 * kStagedConsumerWarps;
+constexpr int kStagedThreads = kStagedConsumers + 32;  // + the producer warp
+static_assert(kTile % (4 * kStagedConsumers) == 0, "whole 4-element chunks per consumer");
+static_assert(kStagedThreads <= 32 * kMaxWarps, "finish_cta's per-warp slots");
+constexpr int kMaxStages = 2;
 constexpr size_t kStagedSmemLimit = 200 * 1024;  // dynamic shared memory per CTA, at most
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
@@ -560,7 +569,7 @@ __global__ void __launch_bounds__(kStagedThreads)
             }
         }
     } else {  // the consumers
-        const int c = threadIdx.x;  // 0 .. 127
+        const int c = threadIdx.x;  // 0 .. kStagedConsumers - 1
         int64_t k = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++k) {
             const int st_i = static_cast<int>(k % stages);
@@ -571,9 +580,9 @@ __global__ void __launch_bounds__(kStagedThreads)
             const int64_t e0 = t * kTile;
             const int64_t len = (range - e0 < kTile) ? range - e0 : kTile;
             const unsigned char* st = smem + static_cast<size_t>(st_i) * a.stage_bytes;
-            const int e_a = 4 * c, e_b = kHalfTile + 4 * c;
-            if (e_a < len) staged_chunk<NT, kBF16>(a, s, st, e_a, a.begin + e0 + e_a, bad, sumsq);
-            if (e_b < len) staged_chunk<NT, kBF16>(a, s, st, e_b, a.begin + e0 + e_b, bad, sumsq);
+#pragma unroll
+            for (int e = 4 * c; e < kTile; e += 4 * kStagedConsumers)
+                if (e < len) staged_chunk<NT, kBF16>(a, s, st, e, a.begin + e0 + e, bad, sumsq);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st_i]);
         }
