@@ -591,30 +591,48 @@ __global__ void __launch_bounds__(kStagedThreads)
     finish_cta(a, bad, sumsq);
 }
 
+// U groups of the first pass of the two-pass form.
+template <int NT, bool kBF16, int U>
+__device__ __forceinline__ void reduce_groups(const StepArgs& a, const Scalars& s,
+                                              const int64_t (&j)[U], unsigned& bad,
+                                              double& sumsq) {
+    float g[U][kVec];
+#pragma unroll
+    for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        float sq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            g[u][e] = __fmul_rn(g[u][e], s.inv);
+            bad |= is_nonfinite(g[u][e]) ? 1u : 0u;
+            sq = fmaf(g[u][e], g[u][e], sq);
+        }
+        sumsq += static_cast<double>(sq);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) store8(a.gws, j[u], g[u]);
+}
+
 // First pass of the two-pass form: reduce-scatter + scale + check, writing the
-// FP32 combined gradient to the workspace.
+// FP32 combined gradient to the workspace.  Two groups per thread in flight,
+// as in the fused kernel.
 template <int NT, bool kBF16>
-__global__ void __launch_bounds__(kThreads) zero_reduce_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) zero_reduce_kernel(const __grid_constant__ StepArgs a) {
     allow_next_launch();
     unsigned bad = 0;
     double sumsq = 0.0;
     const Scalars s = step_scalars(a);
     const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < n8;
-         q += stride) {
-        const int64_t j = a.begin + q * kVec;
-        float g[kVec];
-        combine<NT, kBF16>(a, j, g);
-        float sq = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) {
-            g[e] = __fmul_rn(g[e], s.inv);
-            bad |= is_nonfinite(g[e]) ? 1u : 0u;
-            sq = fmaf(g[e], g[e], sq);
-        }
-        sumsq += static_cast<double>(sq);
-        store8(a.gws, j, g);
+    int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (; q + stride < n8; q += 2 * stride) {
+        const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+        reduce_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
+    }
+    if (q < n8) {
+        const int64_t j[1] = {a.begin + q * kVec};
+        reduce_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -694,10 +712,41 @@ __device__ __forceinline__ void copy_state(const StepArgs& a) {
     }
 }
 
+// U groups of the second pass: Adam + BF16 all-gather from the combined
+// gradient, clipped by coef when the step clips.
+template <int U>
+__device__ __forceinline__ void update_groups(const StepArgs& a, const Scalars& s, float coef,
+                                              const int64_t (&j)[U]) {
+    float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        load8(a.src_master, j[u], p[u]);
+        load8(a.src_m, j[u], m[u]);
+        load8(a.src_v, j[u], v[u]);
+        load8(a.gws, j[u], g[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            const float gs = a.clip ? __fmul_rn(g[u][e], coef) : g[u][e];
+            adam_element(gs, p[u][e], m[u][e], v[u][e], s);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        store8(a.dst_master, j[u], p[u]);
+        store8(a.dst_m, j[u], m[u]);
+        store8(a.dst_v, j[u], v[u]);
+        store_w8(a.dst_w, j[u], p[u]);
+    }
+}
+
 // Second pass of the two-pass form: Adam + BF16 all-gather from the
 // workspace's combined gradient, unless the step was skipped.  A skipped
-// out-of-place step copies src to dst instead.
-__global__ void __launch_bounds__(kThreads) zero_update_kernel(const __grid_constant__ StepArgs a) {
+// out-of-place step copies src to dst instead.  Two groups per thread in
+// flight, as in the fused kernel.
+__global__ void __launch_bounds__(kThreads, 2) zero_update_kernel(const __grid_constant__ StepArgs a) {
     allow_next_launch();
     if (a.ctrl->skip) {
         if (a.dst_master != a.src_master) copy_state(a);
@@ -705,23 +754,14 @@ __global__ void __launch_bounds__(kThreads) zero_update_kernel(const __grid_cons
         const float coef = a.ctrl->clip_coef;
         const Scalars s = step_scalars(a);
         const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-        for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
-             q += stride) {
-            const int64_t j = a.begin + q * kVec;
-            float p[kVec], m[kVec], v[kVec], g[kVec];
-            load8(a.src_master, j, p);
-            load8(a.src_m, j, m);
-            load8(a.src_v, j, v);
-            load8(a.gws, j, g);
-#pragma unroll
-            for (int e = 0; e < kVec; ++e) {
-                const float gs = a.clip ? __fmul_rn(g[e], coef) : g[e];
-                adam_element(gs, p[e], m[e], v[e], s);
-            }
-            store8(a.dst_master, j, p);
-            store8(a.dst_m, j, m);
-            store8(a.dst_v, j, v);
-            store_w8(a.dst_w, j, p);
+        int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+        for (; q + stride < a.n8; q += 2 * stride) {
+            const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+            update_groups<2>(a, s, coef, j);
+        }
+        if (q < a.n8) {
+            const int64_t j[1] = {a.begin + q * kVec};
+            update_groups<1>(a, s, coef, j);
         }
     }
     // A sub-launch chained to the previous one completes only after it: the
