@@ -118,7 +118,8 @@ typedef struct {
 
 /* Outcome of one step, written by the device at the end of the step. */
 typedef struct {
-    int32_t status;           /* ZERO_OK (applied), ZERO_STEP_SKIPPED or ZERO_ERR_TIMEOUT */
+    int32_t status;           /* ZERO_OK (applied), ZERO_STEP_SKIPPED, ZERO_ERR_TIMEOUT or
+                                 ZERO_ERR_POLICY_WINDOW                              */
     uint32_t found_nonfinite; /* 1 if any combined gradient element was inf or NaN        */
     float grad_norm;          /* L2 norm of the combined batch-mean gradient, before clip */
     float clip_coef;          /* factor applied to the gradient (1 without clipping)      */

@@ -86,7 +86,7 @@ def _oracle_check(oracle_mod, grads, N, scale, psi_pad):
 
 
 def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=None,
-                  device_policy=False):
+                  device_policy=False, staging=0):
     from zero_sharded_mixed_04_gb300 import synth
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     wl = synth.WORKLOADS[name]
@@ -100,7 +100,7 @@ def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=
                    skip_on_overflow=wl.skip_on_overflow, bucket_elems=wl.bucket_elems,
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
                    out_of_place=out_of_place, device=dev, master=master,
-                   device_policy=device_policy)
+                   device_policy=device_policy, smem_staging=staging)
     del master
     _free()
     hp = oracle_mod.Hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
@@ -172,9 +172,28 @@ def test_ragged6b_n4(zero_lib, oracle_mod):
     _run_workload(zero_lib, oracle_mod, "ragged6b_n4", out_of_place=False, full_compare=False)
 
 
+def test_ragged6b_n4_staged(zero_lib, oracle_mod):
+    """The TMA-staged one-pass kernel past the 2^31 and 2^32 element
+    boundaries (6e9 parameters)."""
+    _run_workload(zero_lib, oracle_mod, "ragged6b_n4", out_of_place=False, full_compare=False,
+                  staging=zero_lib.ZERO_STAGING_TMA)
+
+
+def test_gpt2small_n4_staged(zero_lib, oracle_mod):
+    _run_workload(zero_lib, oracle_mod, "gpt2small_n4", out_of_place=False, full_compare=True,
+                  staging=zero_lib.ZERO_STAGING_TMA)
+
+
 def test_flat1b_n8_as_benchmarked(zero_lib, oracle_mod):
     """The path bench.py times: out of place, through the plan entry points,
-    with t and the loss scale kept on the device; the injected +inf on step 3
-    must be skipped and halve the scale there."""
+    with t and the loss scale kept on the device and every tile staged in
+    shared memory by TMA; the injected +inf on step 3 must be skipped and halve
+    the scale there."""
+    _run_workload(zero_lib, oracle_mod, "flat1b_n8", out_of_place=True, full_compare=False,
+                  device_policy=True, staging=zero_lib.ZERO_STAGING_TMA)
+
+
+def test_flat1b_n8_register_kernel_with_device_policy(zero_lib, oracle_mod):
+    """bench.py --staging registers: the same path with the register kernel."""
     _run_workload(zero_lib, oracle_mod, "flat1b_n8", out_of_place=True, full_compare=False,
                   device_policy=True)

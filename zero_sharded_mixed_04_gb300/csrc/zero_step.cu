@@ -22,10 +22,16 @@
 // one owner, because every slice is a multiple of 128 elements.
 //
 // The path is bound by HBM bandwidth (about 0.5 flop per byte), so nothing
-// here uses tensor cores.  Each thread moves 16-byte vectors.  Every load of
-// a group is issued before its arithmetic.  The arithmetic uses the explicit
-// round-to-nearest intrinsics, so no multiply-add is ever contracted: each
-// element is rounded operator by operator.
+// here uses tensor cores.  The one-pass step has two kernels that give the
+// same bits:
+//   - zero_fused_kernel: each thread loads 16-byte vectors straight into
+//     registers, two 8-element groups in flight, every load of a group issued
+//     before its arithmetic;
+//   - zero_fused_staged_kernel: one thread per CTA copies each tile into
+//     shared memory with TMA bulk copies, and sixteen warps compute from there.
+// The arithmetic uses the explicit round-to-nearest intrinsics, so no
+// multiply-add is ever contracted: each element is rounded operator by
+// operator.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
