@@ -426,6 +426,22 @@ int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream);
  * w_bf16 + r*S.  They may equally be N separate buffers.
  * ------------------------------------------------------------------------ */
 
+/* Flags of zero3_gather.
+ *   ZERO3_GATHER_OVERLAP_PREVIOUS  the gather may start copying while the
+ *       kernel enqueued right before it on `stream` drains, without waiting
+ *       for it to complete.  Since that kernel may be a gather launched with
+ *       this flag too, which did not wait for its own predecessor either, the
+ *       kernels that may still be running form a chain back to the last
+ *       kernel launched without the flag.  The caller promises that none of
+ *       them writes the shards or reads or writes `view`, except those that
+ *       an event wait enqueued on `stream` before this gather already orders
+ *       before it.  Waits on events stay complete dependencies.  Example: the
+ *       gathers of consecutive layers alternating between two views, each
+ *       view refilled only after an event wait for the use of its previous
+ *       layer (the two-view schedule below).  Without the flag the gather
+ *       begins only after everything before it on the stream has completed. */
+#define ZERO3_GATHER_OVERLAP_PREVIOUS 1u
+
 /* Copies elements [begin, end) of the full flat view into `view`.  Element j
  * is read from shards[j / shard] at offset j % shard.
  *   shards   host array of N device pointers, each ZERO_ALIGN_BYTES-aligned,
@@ -434,13 +450,14 @@ int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream);
  *            layout from zero_init_layout qualifies)
  *   view     device buffer of end - begin BF16 values, ZERO_ALIGN_BYTES-aligned;
  *            it must not overlap a shard
+ *   flags    0 or ZERO3_GATHER_OVERLAP_PREVIOUS
  * Any 0 <= begin <= end <= N * shard is accepted.  A begin that is a multiple
  * of ZERO_BUCKET_ALIGN takes a 16-byte vector path; any other begin takes an
  * element-by-element path.  Enqueued on `stream`.  Returns ZERO_OK, or
  * ZERO_ERR_ARG / ZERO_ERR_ALIGN / ZERO_ERR_OVERLAP / ZERO_ERR_CUDA before
  * anything is enqueued. */
 int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t shard, int64_t begin,
-                 int64_t end, uint16_t* view, void* stream);
+                 int64_t end, uint16_t* view, uint32_t flags, void* stream);
 
 /* Peak bytes one rank holds under ZeRO-3 when the layers, of layer_numel[i]
  * elements in run order, are gathered one ahead into two BF16 views (one in

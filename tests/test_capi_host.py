@@ -295,3 +295,4 @@ def test_zero3_gather_rejects_bad_arguments(zero_lib):
         Z.ZERO_ERR_ALIGN
     assert Z.zero3_gather(shards, 4, 1024, 0, 16, 2 * GB + 64, 0) == Z.ZERO_ERR_OVERLAP
     assert Z.zero3_gather(shards, 4, 1024, 7, 7, None, 0) == Z.ZERO_OK              # empty: nothing
+    assert Z.zero3_gather(shards, 4, 1024, 0, 16, 5 * GB, 0, flags=2) == Z.ZERO_ERR_ARG  # unknown flag

@@ -122,3 +122,29 @@ def test_two_view_schedule_as_a_cuda_graph(zero_lib, oracle_mod):
         for i, (b, e) in enumerate(layers):
             want = oracle_mod.gather_range(oshards, b, e)
             assert np.array_equal(outs[i].cpu().numpy().view(np.uint16), want), f"seed {seed} layer {i}"
+
+
+def test_overlapping_gathers_into_distinct_views(zero_lib, oracle_mod):
+    """Consecutive gathers launched with ZERO3_GATHER_OVERLAP_PREVIOUS into
+    separate views (none touches another's view, all only read the shards):
+    each may start while the previous drains, and every view must still equal
+    the oracle's gather."""
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, shard = 8, 131072
+    rng = np.random.default_rng(77)
+    host = [rng.integers(0, 1 << 16, size=shard).astype(np.uint16) for _ in range(N)]
+    shards = [torch.from_numpy(h.view(np.int16).copy()).to(dev) for h in host]
+    total = N * shard
+    bounds = [0, 40_000, 40_008, 300_016, 300_021, 700_000, 1_000_003, total]
+    layers = list(zip(bounds[:-1], bounds[1:]))
+    views = [torch.full((e - b + 8,), -1, dtype=torch.int16, device=dev) for b, e in layers]
+    for _ in range(3):
+        for i, ((b, e), v) in enumerate(zip(layers, views)):
+            flags = Z.ZERO3_GATHER_OVERLAP_PREVIOUS if i else 0
+            assert Z.zero3_gather(shards, N, shard, b, e, v, None, flags=flags) == Z.ZERO_OK
+    torch.cuda.synchronize()
+    for (b, e), v in zip(layers, views):
+        got = v.cpu().numpy().view(np.uint16)
+        assert np.array_equal(got[:e - b], oracle_mod.gather_range(host, b, e)), (b, e)
+        assert (got[e - b:] == 0xFFFF).all(), "wrote past the range"

@@ -1537,23 +1537,25 @@ struct GatherArgs {
     int64_t seg_len[ZERO_MAX_RANKS];
     int32_t seg_shard[ZERO_MAX_RANKS];
     int32_t segments;
+    int32_t wait_previous;  // 0 under ZERO3_GATHER_OVERLAP_PREVIOUS
 };
 
 constexpr int kGatherUnroll = 4;  // 16-byte vectors in flight per thread
 
 // The gathers are launched as programmatic dependents of whatever precedes
 // them on the stream, so their CTAs are scheduled while that kernel drains.
-// Every thread waits for that kernel to complete before its first access, so
-// the order is the plain stream order for any caller.
-__device__ __forceinline__ void gather_prologue() {
+// Unless the caller declared that kernel independent of this gather
+// (ZERO3_GATHER_OVERLAP_PREVIOUS), every thread waits for it to complete
+// before its first access, which keeps the plain stream order.
+__device__ __forceinline__ void gather_prologue(const GatherArgs& g) {
     allow_next_launch();
-    grid_dependency_wait();
+    if (g.wait_previous) grid_dependency_wait();
 }
 
 // begin is a multiple of kVec, so every segment is a whole number of 8-element
 // groups on both sides; the last segment may end with n % 8 single elements.
 __global__ void __launch_bounds__(kThreads) zero3_gather_vec_kernel(const __grid_constant__ GatherArgs g) {
-    gather_prologue();
+    gather_prologue(g);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     for (int s = 0; s < g.segments; ++s) {
@@ -1579,7 +1581,7 @@ __global__ void __launch_bounds__(kThreads) zero3_gather_vec_kernel(const __grid
 
 // Any begin: element by element (a layer that starts at an odd offset).
 __global__ void __launch_bounds__(kThreads) zero3_gather_elem_kernel(const __grid_constant__ GatherArgs g) {
-    gather_prologue();
+    gather_prologue(g);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < g.n; i += stride) {
         const int64_t j = g.begin + i;
@@ -1591,10 +1593,11 @@ __global__ void __launch_bounds__(kThreads) zero3_gather_elem_kernel(const __gri
 }  // namespace
 
 extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t shard, int64_t begin,
-                            int64_t end, uint16_t* view, void* stream) {
+                            int64_t end, uint16_t* view, uint32_t flags, void* stream) {
     NvtxRange range("zero3_gather");
     if (shards == nullptr || N < 1 || N > ZERO_MAX_RANKS || shard < 0 || shard % kVec != 0 ||
-        begin < 0 || end < begin || end > static_cast<int64_t>(N) * shard)
+        begin < 0 || end < begin || end > static_cast<int64_t>(N) * shard ||
+        (flags & ~ZERO3_GATHER_OVERLAP_PREVIOUS) != 0)
         return ZERO_ERR_ARG;
     const int64_t n = end - begin;
     if (n == 0) return ZERO_OK;
@@ -1614,6 +1617,7 @@ extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t sh
     g.shard = shard;
     g.begin = begin;
     g.n = n;
+    g.wait_previous = (flags & ZERO3_GATHER_OVERLAP_PREVIOUS) ? 0 : 1;
     // cut [begin, end) at shard boundaries
     g.segments = 0;
     for (int64_t at = begin; at < end;) {

@@ -458,8 +458,12 @@ class Zero3Views:
             # before this pass began; the side stream's wait for the caller's
             # stream at the start of the pass already orders them
             self.side.wait_event(self.released[slot])
+        # after the first layer of a pass, the kernel before this gather on the
+        # side stream is the previous layer's gather: it reads the shards and
+        # writes the other view, so this one may start while it drains
+        flags = Z.ZERO3_GATHER_OVERLAP_PREVIOUS if i >= 1 else 0
         Z.check(Z.zero3_gather(self.shards, self.N, self.shard, b, e, self.views[slot],
-                               self.side), "zero3_gather")
+                               self.side, flags=flags), "zero3_gather")
         self.gathered[slot].record(self.side)
 
     def run(self, use, stream=None) -> None:

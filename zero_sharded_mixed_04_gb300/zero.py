@@ -53,6 +53,8 @@ ZERO_STAGING_REGISTERS = 0
 ZERO_STAGING_TMA = 1
 ZERO_STAGING_TMA_TEST_STALL = 2
 
+ZERO3_GATHER_OVERLAP_PREVIOUS = 1
+
 
 class zero_layout(ctypes.Structure):
     _fields_ = [("psi", ctypes.c_int64), ("psi_pad", ctypes.c_int64), ("shard", ctypes.c_int64),
@@ -131,7 +133,7 @@ _lib.zero_plan_end.restype = ctypes.c_int
 _lib.zero_step_noalloc.argtypes = [_P, _i32, _P, _P, _P, _P, _i64, _i32,
                                    ctypes.POINTER(zero_adam_hparams), _f32, _P, _P]
 _lib.zero_step_noalloc.restype = ctypes.c_int
-_lib.zero3_gather.argtypes = [_P, _i32, _i64, _i64, _i64, _P, _P]
+_lib.zero3_gather.argtypes = [_P, _i32, _i64, _i64, _i64, _P, ctypes.c_uint32, _P]
 _lib.zero3_gather.restype = ctypes.c_int
 _lib.zero3_peak_bytes.argtypes = [_P, _i64, _i32, _i32, _i32]
 _lib.zero3_peak_bytes.restype = _i64
@@ -284,10 +286,11 @@ def zero_step_noalloc(grads, grad_dtype: int, master, m, v, w_bf16, psi_pad: int
                                   loss_scale, _addr(result), _stream(stream))
 
 
-def zero3_gather(shards, N: int, shard: int, begin: int, end: int, view, stream=None) -> int:
+def zero3_gather(shards, N: int, shard: int, begin: int, end: int, view, stream=None,
+                 flags: int = 0) -> int:
     """Elements [begin, end) of the full BF16 view, gathered from N shards."""
     arr = (ctypes.c_void_p * max(len(shards), 1))(*[_addr(x) for x in shards])
-    return _lib.zero3_gather(arr, N, shard, begin, end, _addr(view), _stream(stream))
+    return _lib.zero3_gather(arr, N, shard, begin, end, _addr(view), flags, _stream(stream))
 
 
 def zero3_peak_bytes(layer_numel, N: int, grad_bytes: int = 2, optim_bytes: int = 12) -> int:
