@@ -94,6 +94,8 @@ def parse_args(argv=None):
                          "over the workload's layers instead of the step")
     ap.add_argument("--zero3-layer-elems", type=int, default=50_000_000,
                     help="layer size for flat workloads in --zero3-gather")
+    ap.add_argument("--bucket-elems", type=int, default=-1,
+                    help="override the workload's bucket size (0: one bucket, the whole vector)")
     ap.add_argument("--psi", type=int, default=0,
                     help="reduced parameter count of the same workload (profiling captures "
                          "only; the benchmark line is the full size)")
@@ -107,6 +109,9 @@ def select_workload(args):
     if args.psi:
         wl = dataclasses.replace(wl, name=f"{wl.name}[psi={args.psi}]", psi_flat=args.psi,
                                  tensor_sizes=())
+    if args.bucket_elems >= 0:
+        wl = dataclasses.replace(wl, name=f"{wl.name}[bucket={args.bucket_elems}]",
+                                 bucket_elems=args.bucket_elems)
     return wl
 
 
