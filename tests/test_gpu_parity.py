@@ -292,7 +292,7 @@ def test_async_steps_without_host_reads(zero_lib, oracle_mod):
     compare_state(state_to_numpy(opt.state()), ref, exact=True)
 
 
-@pytest.mark.parametrize("N,k,dtype,clip,skip,out_of_place,bucket,wd", [
+ACCUMULATION_CASES = [
     (4, 2, "bf16", 0.0, False, False, 0, 0.0),
     (8, 3, "bf16", 0.0, True, True, 400_000, 0.0),
     (3, 4, "fp32", 0.05, False, False, 262_144, 0.1),
@@ -300,15 +300,14 @@ def test_async_steps_without_host_reads(zero_lib, oracle_mod):
     (4, 5, "bf16", 1.0, True, True, 1_000_000, 0.0),
     (2, 3, "fp32", 0.0, False, True, 0, 0.1),
     (5, 2, "fp32", 0.0, True, True, 262_144, 0.0),
-])
-def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, out_of_place,
-                               bucket, wd):
+]
+
+
+def run_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, out_of_place, bucket, wd,
+                     staging=0):
     """k micro-batches reduce-scattered bucket by bucket into the owner's FP32
     accumulator, then one update; against the oracle's accumulation.  With
-    the skip on, micro-batch 1 of step 2 carries a +inf.  Without clip, and
-    unless an in-place step may be skipped, the last micro-batch is added and
-    applied in one pass (the first, second, sixth and seventh cases; in the
-    seventh the +inf arrives in that last micro-batch)."""
+    the skip on, micro-batch 1 of step 2 carries a +inf."""
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     psi = PSI_MULTI_SWEEP if N >= 4 else PSI_SMALL
@@ -317,7 +316,7 @@ def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, ou
     master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(11)) * 0.02
     opt = ZeroAdam(psi_pad, N, dtype, weight_decay=wd, max_grad_norm=clip, skip_on_overflow=skip,
                    bucket_elems=bucket, loss_scale=256.0, out_of_place=out_of_place, device=dev,
-                   master=master.to(dev), micro_batches=k)
+                   master=master.to(dev), micro_batches=k, smem_staging=staging)
     ref = _oracle_state(master.numpy())
     hp = oracle_mod.Hparams(weight_decay=wd, max_grad_norm=clip)
     o_t = 0
@@ -336,6 +335,15 @@ def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, ou
         compare_state(state_to_numpy(opt.state()), ref, exact=clip == 0.0, tag=f"step {step} ")
     if skip:
         assert o_t == 2
+
+
+@pytest.mark.parametrize("N,k,dtype,clip,skip,out_of_place,bucket,wd", ACCUMULATION_CASES)
+def test_gradient_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, out_of_place,
+                               bucket, wd):
+    """Without clip, and unless an in-place step may be skipped, the last
+    micro-batch is added and applied in one pass (the first, second, sixth and
+    seventh cases; in the seventh the +inf arrives in that last micro-batch)."""
+    run_accumulation(zero_lib, oracle_mod, N, k, dtype, clip, skip, out_of_place, bucket, wd)
 
 
 
