@@ -233,8 +233,15 @@ def read_peaks() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 (first 16 hex digits) of the kernel source's code: comments,
+    trailing spaces and blank lines removed, so that a comment edit does not
+    void the profiles taken on the same code."""
+    with open(KERNEL_SOURCE) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines()]
+    code = "\n".join(line for line in lines if line)
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def profiled_traffic_per_param(kernel: str) -> float | None:
