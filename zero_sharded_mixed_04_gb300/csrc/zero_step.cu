@@ -110,7 +110,7 @@ struct StepArgs {
     float* dst_v;
     uint16_t* dst_w;
     const Scalars* sdev; // device policy: read the step's scalars here instead of s
-    float* gws;          // FP32 combined gradient (two-pass form)
+    float* gws;          // FP32 combined gradient (two-pass form) or accumulator (micro-batches)
     double* partials;    // one FP64 sum of squares per CTA
     Ctrl* ctrl;
     Scalars s;
@@ -165,6 +165,10 @@ __device__ __forceinline__ void adam_element(float g, float& p, float& m, float&
 }
 
 // ------------------------------------------------------------------ vector loads
+//
+// Global memory only: __ldcs / __stcs are the global-space cache-streaming
+// forms (ld.global.cs / st.global.cs).  Shared-memory stages are read with
+// lds_u2 / lds_f4 below.
 
 template <bool kBF16>
 struct GradVec;
