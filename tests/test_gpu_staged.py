@@ -173,3 +173,26 @@ def test_staged_rejects_host_gradients(zero_lib):
     plan.smem_staging = Z.ZERO_STAGING_TMA
     assert Z.zero_plan_begin(plan, None) == Z.ZERO_OK
     assert Z.zero_plan_bucket(plan, 0, n, None, None) == Z.ZERO_ERR_ARG
+
+
+@pytest.mark.parametrize("psi", [1, 7, 1023, 2049])
+def test_staged_tiny_vectors(zero_lib, oracle_mod, psi):
+    """A single partial tile (one to a few hundred 8-element groups), out of
+    place with the skip on and in place without it."""
+    run_parity(zero_lib, oracle_mod, N=4, psi=psi, steps=2, staging=TMA)
+    run_parity(zero_lib, oracle_mod, N=8, psi=psi, steps=3, skip=True, out_of_place=True,
+               bad_step=2, staging=TMA)
+
+
+def test_staged_empty_plan(zero_lib):
+    """An empty vector through the plan with staging: no bucket, the step
+    completes and reports success."""
+    Z = zero_lib
+    hp = Z.make_hparams(skip_on_overflow=True)
+    ws = torch.empty(Z.zero_workspace_bytes(0, hp, False), dtype=torch.uint8, device="cuda")
+    plan = Z.zero_plan()
+    assert Z.zero_plan_init(plan, [None, None], Z.ZERO_GRAD_BF16, None, None, None, None, None,
+                            None, None, None, 0, 2, hp, 1.0, ws, ws.numel()) == Z.ZERO_OK
+    plan.smem_staging = Z.ZERO_STAGING_TMA
+    assert Z.zero_plan_begin(plan, None) == Z.ZERO_OK
+    assert Z.zero_plan_end(plan, None, None) == Z.ZERO_OK
