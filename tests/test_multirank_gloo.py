@@ -59,3 +59,24 @@ def test_reference_arm_only_rank0_prints(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
+    """Rank 0 of the reference arm (the oracle on the host cores) prints one
+    JSON line with the benchmark contract's keys, on the default workload."""
+    import json
+    import bench
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "params/s"
+    assert d["config"]["workload"] == "flat1b_n8" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
