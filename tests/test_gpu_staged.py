@@ -1,6 +1,6 @@
 """GPU parity of the shared-memory-staged one-pass kernel (ZERO_STAGING_TMA).
 
-Each 1024-element tile is copied into a shared-memory stage by TMA bulk copies
+Each 2048-element tile is copied into a shared-memory stage by TMA bulk copies
 and computed from there.  The results must equal the oracle's bit for bit, as
 the register kernel's do.  Sizes give ragged last tiles and several tiles per
 CTA.  The cases cover the rank counts, both gradient types, in place and out
