@@ -1555,7 +1555,13 @@ struct GatherArgs {
     int32_t wait_previous;  // 0 under ZERO3_GATHER_OVERLAP_PREVIOUS
 };
 
-constexpr int kGatherUnroll = 4;  // 16-byte vectors in flight per thread
+// 16-byte vectors in flight per thread, and CTAs of kThreads per SM at most.
+// Measured as CUDA-graph replays of the two-view pass: 2 and 6 gave 0.090 ms
+// per GPT-2-small pass and 0.666 ms per pass of twenty 50M-element layers,
+// against 0.097 and 0.671 ms with 4 vectors and every resident CTA (6 per SM);
+// 1, 4 and 8 vectors with 2 to 8 CTAs per SM were no better.
+constexpr int kGatherUnroll = 2;
+constexpr int kGatherCtasPerSm = 6;
 
 // The gathers are launched as programmatic dependents of whatever precedes
 // them on the stream, so their CTAs are scheduled while that kernel drains.
@@ -1654,6 +1660,8 @@ extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t sh
     const int64_t full = static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, kThreads);
     int64_t grid = (units + kThreads - 1) / kThreads;
     if (grid > full) grid = full;
+    const int64_t cap = static_cast<int64_t>(kGatherCtasPerSm) * sm_count(device);
+    if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
