@@ -490,15 +490,15 @@ def run_ours(args, world, rank, local):
 
 
 def pin_host_grads(grads):
-    """The gradients in one pinned host allocation (the pinned allocator rounds
-    each allocation up to a power of two, so one buffer holds every rank)."""
-    import torch
+    """The gradients in one page-locked host buffer backed by huge pages
+    (hostmem.HostBuffer), every rank's a slice of it."""
+    from zero_sharded_mixed_04_gb300.hostmem import HostBuffer
     n = grads[0].numel()
-    flat = torch.empty(n * len(grads), dtype=grads[0].dtype, pin_memory=True)
-    host = [flat[i * n:(i + 1) * n] for i in range(len(grads))]
+    buf = HostBuffer(n * len(grads), grads[0].dtype)
+    host = [buf.tensor[i * n:(i + 1) * n] for i in range(len(grads))]
     for h, g in zip(host, grads):
         h.copy_(g)
-    return flat, host
+    return buf, host
 
 
 def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
@@ -507,7 +507,7 @@ def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
     (overlapped with the reduction of the previous bucket) and reads the
     step result back to the host."""
     import torch
-    flat, host = host_grads
+    buf, host = host_grads
     slots = opt.make_slots()
     copy_stream = torch.cuda.Stream(dev)
     steps = args.e2e_steps or max(1, min(args.steps, 10))
@@ -549,7 +549,10 @@ def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
     link_gbs = h2d / link_s / 1e9
     dt = group.max(statistics.median(times))
     mean = group.max(sum(times) / len(times))
-    del host, slots, flat, host_grads
+    kind = buf.kind
+    del host, slots, host_grads
+    torch.cuda.synchronize(dev)
+    buf.close()
     return {"value": round(group.sum(float(wl.psi)) / dt, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16, "ms_per_step": round(dt * 1e3, 3),
             "steps": steps, "statistic": "median step",
@@ -557,6 +560,7 @@ def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
             "max_ms_per_step": round(group.max(max(times)) * 1e3, 3),
             "h2d_link_gbs": round(link_gbs, 1),
             "h2d_copies_only_ms": round(link_s * 1e3, 3),
+            "host_buffer": kind,
             "path": "pinned host grads -> two device bucket slots -> zero_plan_bucket; "
                     "result read by the host"}
 

@@ -555,3 +555,25 @@ def test_device_policy_window_miss_changes_nothing(zero_lib, out_of_place):
         assert torch.equal(a, b)
     for a, b in zip(src, before):
         assert torch.equal(a, b)
+
+
+def test_host_buffer_is_page_locked_and_huge_page_backed():
+    """hostmem.HostBuffer: registered with the driver (torch sees it as pinned),
+    asynchronous copies both ways keep the bits, and closing unregisters it."""
+    from zero_sharded_mixed_04_gb300.hostmem import HostBuffer
+    n = 3 * (1 << 20) + 5
+    buf = HostBuffer(n, torch.bfloat16)
+    assert buf.kind == "huge-page mapping, cudaHostRegister"
+    assert buf.tensor.is_pinned() and buf.tensor.numel() == n
+    src = torch.randint(-32768, 32767, (n,), dtype=torch.int16,
+                        generator=torch.Generator().manual_seed(4)).view(torch.bfloat16)
+    buf.tensor.copy_(src)
+    dev = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    dev.copy_(buf.tensor, non_blocking=True)
+    back = HostBuffer(n, torch.bfloat16)
+    back.tensor.copy_(dev, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(back.tensor.view(torch.int16), src.view(torch.int16))
+    buf.close()
+    back.close()
+    assert buf.tensor is None

@@ -16,7 +16,7 @@ from __future__ import annotations
 
 import importlib
 
-_SUBMODULES = ("zero", "synth", "build", "optim")
+_SUBMODULES = ("zero", "synth", "build", "optim", "hostmem")
 
 
 def __getattr__(name):

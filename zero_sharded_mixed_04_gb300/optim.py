@@ -90,8 +90,13 @@ class ZeroAdam:
         # host_grad_accum: the owner's FP32 gradient shard (or accumulator) lives
         # in pinned host memory and the kernels reach it over the host link;
         # steps then go through the plan entry points
-        self.grad_accum = (torch.zeros(psi_pad, dtype=torch.float32, pin_memory=True)
-                           if host_grad_accum else None)
+        self._grad_accum_buf = None
+        self.grad_accum = None
+        if host_grad_accum:
+            from .hostmem import HostBuffer
+            self._grad_accum_buf = HostBuffer(psi_pad, torch.float32)
+            self.grad_accum = self._grad_accum_buf.tensor
+            self.grad_accum.zero_()
         self.ws_bytes = (Z.ZERO_WORKSPACE_CONTROL_BYTES if host_grad_accum else
                          Z.zero_workspace_bytes(psi_pad, self.hp, not out_of_place))
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
