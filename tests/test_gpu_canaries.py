@@ -4,6 +4,7 @@ Each device buffer is carved from a larger allocation, with 4 KiB guard
 regions filled with a pattern on both sides.  Steps of every form run, and
 then the guards must be intact:
   - the one-pass, two-pass and out-of-place steps;
+  - the one-pass step staged in shared memory by TMA, in and out of place;
   - clipping and accumulation;
   - the device policy;
   - the ZeRO-3 gather.
@@ -38,7 +39,7 @@ class Guarded:
 
 
 @pytest.mark.parametrize("form", ["one_pass", "two_pass_skip", "out_of_place_clip", "accumulate",
-                                  "device_policy"])
+                                  "device_policy", "staged", "staged_out_of_place_skip"])
 def test_guards_intact_after_steps(zero_lib, form):
     Z = zero_lib
     dev = torch.device("cuda:0")
@@ -51,9 +52,10 @@ def test_guards_intact_after_steps(zero_lib, form):
            Guarded(n, torch.float32, dev, torch.zeros(n, device=dev)),
            Guarded(n, torch.float32, dev, torch.zeros(n, device=dev)),
            Guarded(n, torch.int16, dev, torch.zeros(n, dtype=torch.int16, device=dev))]
-    out_of_place = form in ("out_of_place_clip", "device_policy")
+    out_of_place = form in ("out_of_place_clip", "device_policy", "staged_out_of_place_skip")
     dst = [Guarded(n, x.t.dtype, dev, torch.zeros_like(x.t)) for x in src] if out_of_place else src
-    hp = Z.make_hparams(skip_on_overflow=form in ("two_pass_skip", "device_policy"),
+    hp = Z.make_hparams(skip_on_overflow=form in ("two_pass_skip", "device_policy",
+                                                  "staged_out_of_place_skip"),
                         max_grad_norm=0.1 if form == "out_of_place_clip" else 0.0,
                         micro_batches=k, bucket_elems=4 * 128 * 64)
     ws_bytes = Z.zero_workspace_bytes(n, hp, not out_of_place)
@@ -64,6 +66,8 @@ def test_guards_intact_after_steps(zero_lib, form):
                             *[x.t for x in src], *[x.t for x in dst], n, N, hp, 1.0, ws.t,
                             ws_bytes) == Z.ZERO_OK
     plan.overlap_buckets = 1
+    if form.startswith("staged"):
+        plan.smem_staging = Z.ZERO_STAGING_TMA
     if form == "device_policy":
         pol_mem = torch.zeros(ctypes.sizeof(Z.zero_device_policy), dtype=torch.uint8,
                               pin_memory=True)
