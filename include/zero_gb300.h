@@ -283,20 +283,20 @@ typedef struct {
  *                           (the N gradient chunks and the master/m/v chunks)
  *                           into one of two shared-memory stages with TMA bulk
  *                           copies; sixteen warps compute from shared memory.
- *                           The chunks streaming through two slots (one in use,
- *                           one loading) is the DP-ZeRO blog's two-buffer
+ *                           Streaming the chunks through two slots, one in use
+ *                           and one loading, is the DP-ZeRO blog's two-buffer
  *                           pattern.  Needs 2 * (N * 2048 * g + 24576) bytes of
  *                           shared memory per CTA, at most 200 KB (g = 2 for
- *                           BF16 gradients, 4 for FP32: N <= 18 and N <= 9), and the
- *                           gradients and src master/m/v in device memory (the
- *                           copies read no pinned host or managed memory);
- *                           otherwise zero_plan_bucket returns ZERO_ERR_ARG.
- *                           Every wait in
- *                           the kernel gives up after about a second: the step
- *                           then ends with status ZERO_ERR_TIMEOUT and is not
- *                           applied (out of place, dst is restored from src; in
- *                           place, the state of the tiles not reached is left
- *                           as it was and the rest is updated).
+ *                           BF16 gradients, 4 for FP32: N <= 18 and N <= 9),
+ *                           and the gradients and src master/m/v in device
+ *                           memory (the copies read no pinned host or managed
+ *                           memory); otherwise zero_plan_bucket returns
+ *                           ZERO_ERR_ARG.  Every wait in the kernel gives up
+ *                           after about a second: the step then ends with
+ *                           status ZERO_ERR_TIMEOUT and is not applied (out of
+ *                           place, dst is restored from src; in place, the
+ *                           tiles not reached keep their state and the rest
+ *                           are updated).
  *   ZERO_STAGING_TMA_TEST_STALL  as ZERO_STAGING_TMA, except that CTA 0 of every
  *                           launch never copies its first tile, so that waits
  *                           run out: for testing the timeout path only.
