@@ -494,7 +494,9 @@ def pin_host_grads(grads):
     (hostmem.HostBuffer), every rank's a slice of it."""
     from zero_sharded_mixed_04_gb300.hostmem import HostBuffer
     n = grads[0].numel()
-    buf = HostBuffer(n * len(grads), grads[0].dtype)
+    # every rank on this node allocates one such buffer at about the same time
+    ranks_here = int(os.environ.get("LOCAL_WORLD_SIZE", os.environ.get("WORLD_SIZE", "1")))
+    buf = HostBuffer(n * len(grads), grads[0].dtype, share=ranks_here)
     host = [buf.tensor[i * n:(i + 1) * n] for i in range(len(grads))]
     for h, g in zip(host, grads):
         h.copy_(g)
