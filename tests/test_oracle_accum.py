@@ -9,6 +9,8 @@
   rounding noise.
 * A non-finite value in any micro-batch makes the accumulated gradient
   non-finite, so the step is skipped.
+* Hand-worked FP32 cases whose bits depend on the micro-batches being added
+  in order, to an accumulator that starts from +0.
 """
 import numpy as np
 import pytest
@@ -112,3 +114,48 @@ def test_nonfinite_in_any_micro_batch_skips(oracle_mod):
     assert res["found_nonfinite"] and not res["applied"]
     for x, y in zip(st, before):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_micro_batches_add_in_order(oracle_mod):
+    """N = 1, k = 4, loss scale 1, so each micro-batch adds its gradient times
+    fp32(1/4) = 0.25 (exact).  Micro-batch values (T, 1, -T, 1) with T = 2**27
+    add 2**25, 0.25, -2**25, 0.25.  In micro-batch order from +0:
+    2**25, 2**25 + 0.25 = 2**25 (the FP32 spacing there is 4), +0, 0.25.
+    Reversed: 0.25, -2**25 (spacing 2 just below), -2**25, +0.  In pairs:
+    2**25 + -2**25 = +0.  m after one step from m = 0 is fp32(0.1) * g."""
+    T = float(2 ** 27)
+    n = 128
+    micro = []
+    for x in (T, 1.0, -T, 1.0):
+        g = np.zeros(n, np.float32)
+        g[0] = x
+        micro.append([g])
+    master, m, v, w = (np.zeros(n, np.float32), np.zeros(n, np.float32),
+                       np.zeros(n, np.float32), np.zeros(n, np.uint16))
+    res = oracle_mod.zero_step_accum(micro, master, m, v, w, oracle_mod.Hparams(), 1, 1.0)
+    assert res["sumsq"] == 0.0625
+    assert m[0] == np.float32(1.0 - 0.9) * np.float32(0.25)
+    assert not m[1:].any()
+
+
+def test_accumulator_starts_from_positive_zero(oracle_mod):
+    """N = 1, k = 2, loss scale 1, FP32 gradients equal to -2**-149 (the
+    negative subnormal of least magnitude) in both micro-batches.  Each
+    contribution is -2**-149 * fp32(1/2) = -2**-150, a tie between -0 and
+    -2**-149 that rounds to the even -0.  From +0 the accumulator is
+    +0 + -0 = +0 twice over; started from the first contribution it would be
+    -0.  With m = master = -0 before the step: m = 0.9 * -0 + 0.1 * +0 = +0 and
+    master = -0 - lr * (+0 / eps) = -0 (a -0 gradient gives m = -0, master = +0)."""
+    n = 2 * 128
+    tiny = np.float32(-(2.0 ** -149))
+    assert tiny != 0 and np.float32(tiny * np.float32(0.5)) == 0
+    micro = [[np.full(n, tiny, np.float32)] for _ in range(2)]
+    master = np.full(n, -0.0, np.float32)
+    m = np.full(n, -0.0, np.float32)
+    v = np.zeros(n, np.float32)
+    w = np.zeros(n, np.uint16)
+    res = oracle_mod.zero_step_accum(micro, master, m, v, w, oracle_mod.Hparams(), 1, 1.0)
+    assert res["applied"] and res["sumsq"] == 0.0
+    assert (m.view(np.uint32) == 0).all()
+    assert (master.view(np.uint32) == 0x80000000).all()
+    assert (w == 0x8000).all()

@@ -12,6 +12,9 @@ fail.  The mistakes are the kind a restatement of the method could contain.
   - Wrong step-wide rules: a skip that does not skip, a clip coefficient not
     capped at 1, weight decay without the learning rate.
   - A wrong ledger formula.
+  - A wrong summation order or start: the ranks added in reverse or in
+    pairs, a sum started from rank 0's value instead of +0, and the same two
+    slips for the micro-batches of an accumulated step.
 """
 import concurrent.futures
 import os
@@ -56,6 +59,24 @@ MUTANTS = {
     "peak_forgets_prefetched_view": (
         "int64_t pair = layer_numel[i] + (i + 1 < n_layers ? layer_numel[i + 1] : 0);",
         "int64_t pair = layer_numel[i];"),
+    "reduction_order_reversed": (
+        "for (int32_t i = 0; i < N; ++i)\n        a = a + orc_load_grad(grads[i], dtype, idx);",
+        "for (int32_t i = N - 1; i >= 0; --i)\n        a = a + orc_load_grad(grads[i], dtype, idx);"),
+    "reduction_in_pairs": (
+        "for (int32_t i = 0; i < N; ++i)\n        a = a + orc_load_grad(grads[i], dtype, idx);",
+        "for (int32_t i = 0; i + 1 < N; i += 2)\n"
+        "        a = a + (orc_load_grad(grads[i], dtype, idx) + orc_load_grad(grads[i + 1], dtype, idx));\n"
+        "    if (N % 2)\n        a = a + orc_load_grad(grads[N - 1], dtype, idx);"),
+    "reduction_starts_from_rank0": (
+        "float a = 0.0f;\n    for (int32_t i = 0; i < N; ++i)",
+        "float a = orc_load_grad(grads[0], dtype, idx);\n    for (int32_t i = 1; i < N; ++i)"),
+    "micro_batches_reversed": (
+        "for (int32_t mb = 0; mb < k; ++mb)",
+        "for (int32_t mb = k - 1; mb >= 0; --mb)"),
+    "accumulator_starts_from_first_micro_batch": (
+        "        acc[j] = 0.0f;\n    for (int32_t mb = 0; mb < k; ++mb)",
+        "        acc[j] = orc_reduce_element(grads, dtype, N, j, inv);\n"
+        "    for (int32_t mb = 1; mb < k; ++mb)"),
     "accumulation_mean_without_k": (
         "float inv = (float)(1.0 / ((double)N * (double)k * loss_scale));",
         "float inv = (float)(1.0 / ((double)N * loss_scale));"),
