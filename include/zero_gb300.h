@@ -216,7 +216,8 @@ int zero_step_into(const void* const* grads, int32_t grad_dtype,
  * Real systems group gradients into buckets and synchronise the ready ones
  * while later layers are still running backward.  The DP-ZeRO blog, section
  * "offloading the shard to the CPU: two buffers", streams gradient chunks
- * through two device slots: one in use, one loading.  A plan lets a caller do
+ * through two device slots that alternate: while the kernel reads one, the
+ * next chunk is copied into the other.  A plan lets a caller do
  * either.  It enqueues the reduce-scatter one bucket at a time, in flat order,
  * each bucket as soon as its gradients are ready.  A bucket's gradients may sit
  * anywhere, for example in one of two staging slots.  The owner update is
@@ -283,9 +284,9 @@ typedef struct {
  *                           (the N gradient chunks and the master/m/v chunks)
  *                           into one of two shared-memory stages with TMA bulk
  *                           copies; sixteen warps compute from shared memory.
- *                           Streaming the chunks through two slots, one in use
- *                           and one loading, is the DP-ZeRO blog's two-buffer
- *                           pattern.  Needs 2 * (N * 2048 * g + 24576) bytes of
+ *                           Alternating the chunks between two slots, one
+ *                           computed from while the other fills, is the DP-ZeRO
+ *                           blog's two-buffer pattern.  Needs 2 * (N * 2048 * g + 24576) bytes of
  *                           shared memory per CTA, at most 200 KB (g = 2 for
  *                           BF16 gradients, 4 for FP32: N <= 18 and N <= 9),
  *                           and the gradients and src master/m/v in device
@@ -524,7 +525,10 @@ uint64_t zero_launch_count(void);
  * All calls on a device share the one array, which keeps the last step's
  * contents.  Two calls whose work overlaps on the GPU race on it: from
  * different streams or host threads, order them (one stream, or events)
- * yourself.  Returns as zero_step does, or ZERO_ERR_TOO_LARGE. */
+ * yourself.  Returns as zero_step does, or ZERO_ERR_TOO_LARGE.  zero_step's
+ * argument and alignment checks come first: a call they reject gets their
+ * ZERO_ERR_ARG or ZERO_ERR_ALIGN whatever its size.  ZERO_ERR_OVERLAP is
+ * checked after the size. */
 #define ZERO_NOALLOC_MAX_TWO_PASS_ELEMS 4194304
 #define ZERO_NOALLOC_SCRATCH_BYTES (16640 + 4 * ZERO_NOALLOC_MAX_TWO_PASS_ELEMS)
 int zero_step_noalloc(const void* const* grads, int32_t grad_dtype,

@@ -296,3 +296,29 @@ def test_zero3_gather_rejects_bad_arguments(zero_lib):
     assert Z.zero3_gather(shards, 4, 1024, 0, 16, 2 * GB + 64, 0) == Z.ZERO_ERR_OVERLAP
     assert Z.zero3_gather(shards, 4, 1024, 7, 7, None, 0) == Z.ZERO_OK              # empty: nothing
     assert Z.zero3_gather(shards, 4, 1024, 0, 16, 5 * GB, 0, flags=2) == Z.ZERO_ERR_ARG  # unknown flag
+
+
+def _noalloc(Z, N=4, psi_pad=4 * 128 * 4, hp=None, dtype=None, master=1 * GB):
+    hp = hp or Z.make_hparams()
+    grads = [6 * GB + i * GB // 4 for i in range(N)]
+    return Z.zero_step_noalloc(grads, Z.ZERO_GRAD_BF16 if dtype is None else dtype, master,
+                               2 * GB, 3 * GB, 4 * GB, psi_pad, N, hp, 1.0, None, 0)
+
+
+def test_noalloc_argument_errors_come_before_the_size_check(zero_lib):
+    """zero_step_noalloc rejects what zero_step rejects with zero_step's code,
+    whatever the size; only a call that passes those checks is held against
+    the fixed array.  Fake addresses: nothing here reaches the GPU."""
+    Z = zero_lib
+    big = Z.ZERO_NOALLOC_MAX_TWO_PASS_ELEMS + 4 * 128   # too large for the two-pass form
+    two_pass = Z.make_hparams(skip_on_overflow=True)
+    assert _noalloc(Z, psi_pad=big, hp=two_pass) == Z.ZERO_ERR_TOO_LARGE
+    assert _noalloc(Z, psi_pad=big + 8, hp=two_pass) == Z.ZERO_ERR_ARG       # not a multiple of N*128
+    assert _noalloc(Z, psi_pad=big, hp=Z.make_hparams(skip_on_overflow=True, micro_batches=2)) \
+        == Z.ZERO_ERR_ARG                                                    # one batch only
+    assert _noalloc(Z, N=0, psi_pad=big, hp=two_pass) == Z.ZERO_ERR_ARG
+    assert _noalloc(Z, psi_pad=big, hp=two_pass, dtype=9) == Z.ZERO_ERR_ARG
+    assert _noalloc(Z, psi_pad=big, hp=Z.make_hparams(skip_on_overflow=True, lr=-1.0)) \
+        == Z.ZERO_ERR_ARG
+    assert _noalloc(Z, psi_pad=big, hp=two_pass, master=None) == Z.ZERO_ERR_ARG
+    assert _noalloc(Z, psi_pad=big, hp=two_pass, master=1 * GB + 4) == Z.ZERO_ERR_ALIGN

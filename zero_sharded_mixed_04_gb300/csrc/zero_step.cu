@@ -374,9 +374,9 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
 // (cp.async.bulk), counted in the stage's "full" mbarrier.  Sixteen consumer
 // warps wait on it, compute from shared memory, store the results straight to
 // HBM and arrive on the stage's "empty" mbarrier, which the producer waits on
-// before it refills the stage.  Two stages per CTA: one tile is computed while
-// the next loads, the two-slot buffer (one in use, one loading) of the offload
-// pattern, inside a kernel.
+// before it refills the stage.  Two stages per CTA: one tile is computed from
+// one stage while the next tile streams into the other, the offload pattern's
+// pair of alternating slots moved inside a kernel.
 //
 // Measured on Psi = 1e9, N = 8 BF16 (interleaved runs on one GPU, against the
 // register kernel at 5.94 ms per step): 2048-element tiles, 16 consumer warps
@@ -386,9 +386,10 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
 // not.
 //
 // Every wait is bounded by the global timer.  A wait that gives up sets
-// ctrl->timeout; the producer then waits (again bounded) for the copies it
-// issued, so that no copy is still landing in shared memory when the CTA
-// exits, and the step ends with ZERO_ERR_TIMEOUT.
+// ctrl->timeout, and the step ends with ZERO_ERR_TIMEOUT.  Before it leaves,
+// the producer always waits (again bounded) for the copies it issued, so that
+// no copy is still landing in shared memory when the CTA exits, whether the
+// wait that gave up was its own or a consumer's.
 //
 // Consumer thread c owns the 4-element chunks starting at 4c, 4c + 4C,
 // 4c + 8C, ... of a tile (C consumer threads), so each shared-memory load of a
@@ -583,10 +584,15 @@ __global__ void __launch_bounds__(kStagedThreads)
                 bulk_load(state + kTile * 4, a.src_m + j, sb, &full[st_i], once);
                 bulk_load(state + 2 * kTile * 4, a.src_v + j, sb, &full[st_i], once);
             }
-            if (timed_out) {
-                // let every copy already issued land before the CTA may exit
-                for (int64_t kk = (k > stages ? k - stages : 0); kk < k; ++kk)
-                    mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
+            // Let every copy this thread issued land before the CTA may exit,
+            // whichever wait (its own or a consumer's) gave up.  A tile older
+            // than the last `stages` was consumed before its stage was refilled,
+            // so only those last tiles can still be in flight.  No arrival
+            // follows them on their "full" barriers, so on the normal path
+            // these waits see phases that have completed or are about to.
+            for (int64_t kk = (k > stages ? k - stages : 0); kk < k; ++kk) {
+                if (a.test_stall && blockIdx.x == 0 && kk == 0) continue;  // never issued
+                mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
             }
         }
     } else {  // the consumers
@@ -1721,7 +1727,17 @@ extern "C" int zero_step_noalloc(const void* const* grads, int32_t grad_dtype, f
                                  float* m, float* v, uint16_t* w_bf16, int64_t psi_pad, int32_t N,
                                  const zero_adam_hparams* hp, float loss_scale,
                                  zero_step_result* result, void* stream) {
-    if (hp == nullptr || psi_pad < 0) return ZERO_ERR_ARG;
+    // zero_step's own argument and alignment checks come first, on the host.
+    // Run without a workspace, a call whose arguments pass them all stops at
+    // the workspace check; only then is the size held against the array.
+    if (master == nullptr && psi_pad > 0) return ZERO_ERR_ARG;
+    if (hp == nullptr || micro_batches_of(hp) > 1) return ZERO_ERR_ARG;
+    {
+        zero_plan probe;
+        const int rc = plan_init(&probe, grads, grad_dtype, master, m, v, w_bf16, master, m, v,
+                                 w_bf16, psi_pad, N, hp, loss_scale, nullptr, 0, false);
+        if (rc != ZERO_ERR_WORKSPACE) return rc;
+    }
     if (workspace_bytes(psi_pad, hp, true) > ZERO_NOALLOC_SCRATCH_BYTES) return ZERO_ERR_TOO_LARGE;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
