@@ -196,12 +196,12 @@ int orc_gather_range(const uint16_t* const* shards, int32_t N, int64_t shard, in
 
 /* Peak bytes one rank holds under ZeRO-3 when the layers (in run order,
  * layer_numel[i] elements each) are gathered one ahead into two temporary
- * BF16 views -- one in use, one being prefetched ([DPZERO "offloading the
- * shard to the CPU: two buffers"]) -- and each view is released after its
- * layer ran: the persistent ZeRO-3 subtotal plus the largest pair of
- * neighbouring layers alive together.  The pages stress that the persistent
- * subtotal is not the peak ([RC-T2 b2, N47]); activations and communication
- * buffers are left out, as in the ledger. */
+ * BF16 views -- the current layer's, and the next layer's being gathered
+ * ([DPZERO "offloading the shard to the CPU: two buffers"]) -- and each view
+ * is released after its layer ran: the persistent ZeRO-3 subtotal plus the
+ * largest pair of neighbouring layers alive together.  The pages stress that
+ * the persistent subtotal is not the peak ([RC-T2 b2, N47]); activations and
+ * communication buffers are left out, as in the ledger. */
 int64_t orc_zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers, int32_t N,
                              int32_t grad_bytes, int32_t optim_bytes)
 {

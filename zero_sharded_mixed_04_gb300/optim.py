@@ -266,7 +266,7 @@ class ZeroAdam:
     # ---------------------------------------------------------------- host gradients
     def make_slots(self, bucket_elems: int | None = None) -> list[list[torch.Tensor]]:
         """Two device staging slots, each holding one bucket of all N ranks'
-        gradients: the two-buffer pattern (one slot in use, one loading)."""
+        gradients: the two-buffer pattern (one slot read while the other refills)."""
         b = bucket_elems or self.hp.bucket_elems or self.psi_pad
         dt = torch.bfloat16 if self.grad_dtype == Z.ZERO_GRAD_BF16 else torch.float32
         return [[torch.empty(b, dtype=dt, device=self.device) for _ in range(self.N)]
