@@ -4,11 +4,14 @@ flat1m_n4 and gpt2small_n4 are compared with the oracle over the whole
 vector, every step.  The three large workloads do not fit the host.  For
 each step the oracle reads every rank's gradient from the device once, in
 chunks on host threads, to form the step-wide overflow flag and norm itself.
-It then steps sampled windows of the vector:
+It then steps sampled windows of 2^20 elements:
   - the first and last elements of every owner's slice;
   - the ragged tail and the padding;
   - the 2^31 and 2^32 element boundaries;
-  - bucket edges, the injected +inf, and seeded random windows.
+  - bucket edges and the injected +inf;
+  - the boundaries between the launches a bucket (or the whole vector) is
+    split into;
+  - 64 seeded random windows.
 It compares each window with the device state, element by element.
 """
 from __future__ import annotations
@@ -26,7 +29,8 @@ from parity_util import compare_result, compare_state, state_to_numpy
 
 pytestmark = pytest.mark.gpu
 
-WIN = 1 << 16
+WIN = 1 << 20
+N_RANDOM = 64
 CHUNK = 1 << 24
 THREADS = max(1, min(16, os.cpu_count() or 1))
 
@@ -36,7 +40,18 @@ def _free():
     torch.cuda.empty_cache()
 
 
-def _windows(wl, psi_pad, shard, extra=(), n_random=8, seed=0):
+def _launch_splits(b0, b1):
+    """Where the library splits the range [b0, b1) of one pass into kernel
+    launches: near-equal parts of at most 2^22 elements, each part a multiple
+    of 256 elements except the last."""
+    groups = (b1 - b0) // 8
+    parts = -(-(groups * 8) // (1 << 22))
+    per = -(-groups // parts)
+    per = -(-per // 32) * 32
+    return [b0 + k * per * 8 for k in range(1, parts) if k * per < groups]
+
+
+def _windows(wl, psi_pad, shard, extra=(), n_random=N_RANDOM, seed=0):
     wins = []
     for r in range(wl.N):
         wins += [(r * shard, r * shard + WIN), ((r + 1) * shard - WIN, (r + 1) * shard)]
@@ -44,11 +59,22 @@ def _windows(wl, psi_pad, shard, extra=(), n_random=8, seed=0):
     for edge in (1 << 31, 1 << 32):
         if edge + WIN < psi_pad:
             wins.append((edge - WIN // 2, edge + WIN // 2))
+    splits = []
     if wl.bucket_elems:
         for k in (1, 2, 17, psi_pad // wl.bucket_elems):
             e = k * wl.bucket_elems
             if WIN < e < psi_pad - WIN:
                 wins.append((e - WIN // 2, e + WIN // 2))
+        # every launch boundary inside the first bucket and one in the middle
+        for k in (0, 17):
+            b0 = k * wl.bucket_elems
+            splits += _launch_splits(b0, min(psi_pad, b0 + wl.bucket_elems))
+    else:
+        cuts = _launch_splits(0, psi_pad)
+        near = [c for c in cuts for edge in (1 << 31, 1 << 32) if abs(c - edge) < (1 << 22)]
+        splits += cuts[:3] + near + cuts[-2:]
+    for c in splits:
+        wins.append((c - WIN // 2, c + WIN // 2))
     for c in extra:
         wins.append((max(0, c - WIN // 2), min(psi_pad, c + WIN // 2)))
     rng = np.random.Generator(np.random.Philox(seed))
@@ -133,11 +159,14 @@ def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=
         compare_result(res, ores)
         if wl.inject_inf_step:
             assert res["applied"] == (step != wl.inject_inf_step)
-        for w in wins:
+        def step_one(w):
             r = ref[w]
             oracle_mod.step_window(gw[w], r["master"], r["m"], r["v"], r["w"], hp, o_t + 1,
                                    o_scale, applied, coef)
-            compare_state(state_to_numpy(opt.state(), *w), r, exact, offset=w[0],
+        with concurrent.futures.ThreadPoolExecutor(THREADS) as ex:
+            list(ex.map(step_one, wins))
+        for w in wins:
+            compare_state(state_to_numpy(opt.state(), *w), ref[w], exact, offset=w[0],
                           tag=f"{name} step {step} ")
         if applied:
             o_t += 1
