@@ -275,6 +275,9 @@ typedef struct {
                                           ZERO_STAGING_REGISTERS (0, as zero_plan_init
                                           leaves it) or ZERO_STAGING_TMA.  Set it between
                                           zero_plan_init and the first zero_plan_bucket.  */
+    void* current_set;                 /* ping-pong sets (zero_plan_set_pingpong): the
+                                          device address of the caller's current-set
+                                          word; NULL (as zero_plan_init leaves it) = off */
 } zero_plan;
 
 /* Values of zero_plan.smem_staging.
@@ -378,6 +381,35 @@ typedef struct {
  * zero_plan_begin.  Returns ZERO_OK or ZERO_ERR_ARG. */
 int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* policy, int64_t t_first,
                                 int32_t t_count);
+
+/* ------------------------------------------------------------------------
+ * Ping-pong state sets.  An out-of-place step reads one full set of
+ * master/m/v/w and writes the other.  Normally the caller swaps the two sets
+ * after every step, and a skipped step must therefore copy the old state into
+ * the other set (28 bytes per parameter), because the caller will read it
+ * from there.  With ping-pong sets the device keeps, in one int32 word, which
+ * set is current.  A step reads the current set and writes the other; when
+ * the step applies, the device flips the word; when it is skipped (overflow,
+ * a t outside the device policy's window, a timed-out wait) the word and the
+ * current set stay as they were and nothing is copied.  The skip costs no
+ * more than the pass that found the overflow.  (Not on the pages; a skipped
+ * step is this library's reading of overflow handling.)
+ * ------------------------------------------------------------------------ */
+
+/* Makes the plan's step use ping-pong sets.  Set 0 is the plan's src_* buffers
+ * and set 1 its dst_* buffers; both are read and written, so the plan must be
+ * out of place with src_w_bf16 given, and no buffer of either set may overlap
+ * another buffer of the step.  *current_set is a caller-owned int32 (0 or 1;
+ * any non-zero value counts as 1), 4-byte aligned and device-addressable:
+ * device memory, or pinned host memory the host may read once the step has
+ * completed.  The step reads it once at its start (in zero_plan_begin's
+ * prologue) and, if the step applies, stores the other set's index into it
+ * when the step ends.  The caller finds the post-step state, and so the
+ * current BF16 working-weight view, in the set it names.  Call between
+ * zero_plan_init(_ex) and zero_plan_begin.  With ZERO_STAGING_TMA both sets'
+ * master/m/v must be in device memory (zero_plan_bucket returns ZERO_ERR_ARG
+ * otherwise).  Returns ZERO_OK, ZERO_ERR_ARG or ZERO_ERR_OVERLAP. */
+int zero_plan_set_pingpong(zero_plan* plan, int32_t* current_set);
 
 /* Starts the step: clears the control block on `stream`. */
 int zero_plan_begin(zero_plan* plan, void* stream);

@@ -322,3 +322,39 @@ def test_noalloc_argument_errors_come_before_the_size_check(zero_lib):
         == Z.ZERO_ERR_ARG
     assert _noalloc(Z, psi_pad=big, hp=two_pass, master=None) == Z.ZERO_ERR_ARG
     assert _noalloc(Z, psi_pad=big, hp=two_pass, master=1 * GB + 4) == Z.ZERO_ERR_ALIGN
+
+
+def test_pingpong_argument_checks(zero_lib):
+    """zero_plan_set_pingpong wants an initialised out-of-place plan whose two
+    sets are complete and disjoint.  Fake addresses: every call here is
+    rejected before any CUDA call."""
+    Z = zero_lib
+    N, n = 4, 4 * 128 * 4
+    grads = [6 * GB + i * GB // 4 for i in range(N)]
+    hp = Z.make_hparams(skip_on_overflow=True)
+    ws = 5 * GB
+    wsb = Z.zero_workspace_bytes(n, hp, False)
+    word = 11 * GB
+
+    def plan_of(src, dst, state=None):
+        plan = Z.zero_plan()
+        rc = Z.zero_plan_init(plan, grads, Z.ZERO_GRAD_BF16, *src, *dst, n, N, hp, 1.0, ws, wsb)
+        assert rc == Z.ZERO_OK
+        return plan
+
+    src = [1 * GB, 2 * GB, 3 * GB, 4 * GB]
+    dst = [12 * GB, 13 * GB, 14 * GB, 15 * GB]
+    plan = Z.zero_plan()
+    assert Z.zero_plan_set_pingpong(plan, word) == Z.ZERO_ERR_ARG          # not initialised
+    p_in = Z.zero_plan()
+    assert Z.zero_plan_init(p_in, grads, Z.ZERO_GRAD_BF16, *src, *src, n, N,
+                            Z.make_hparams(), 1.0, ws,
+                            Z.zero_workspace_bytes(n, Z.make_hparams(), True)) == Z.ZERO_OK
+    assert Z.zero_plan_set_pingpong(p_in, word) == Z.ZERO_ERR_ARG          # in place
+    p = plan_of(src, dst)
+    assert Z.zero_plan_set_pingpong(p, None) == Z.ZERO_ERR_ARG
+    assert Z.zero_plan_set_pingpong(p, word + 2) == Z.ZERO_ERR_ARG         # misaligned
+    # a src buffer that overlaps a gradient is fine while src is only read,
+    # not once ping-pong makes it an output too
+    p = plan_of([grads[1], 2 * GB, 3 * GB, 4 * GB], dst)
+    assert Z.zero_plan_set_pingpong(p, word) == Z.ZERO_ERR_OVERLAP

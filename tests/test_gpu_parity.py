@@ -49,7 +49,7 @@ def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, 
                clip=0.0, skip=False, out_of_place=False, bucket=0, loss_scale=1.0,
                dynamic=False, growth_interval=2000, sigma=1e-3, bad_step=0, bad_value=np.inf,
                seed=1234, api="step", per_bucket_events=False, host_accum=False, staging=0,
-               device_policy=False):
+               device_policy=False, pingpong=False):
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     unit = N * 128
@@ -62,7 +62,8 @@ def run_parity(zero_lib, oracle_mod, *, N, psi, dtype="bf16", steps=3, lr=1e-3, 
                    skip_on_overflow=skip, bucket_elems=bucket, loss_scale=loss_scale,
                    dynamic_loss_scale=dynamic, growth_interval=growth_interval,
                    out_of_place=out_of_place, device=dev, master=master.to(dev),
-                   host_grad_accum=host_accum, smem_staging=staging, device_policy=device_policy)
+                   host_grad_accum=host_accum, smem_staging=staging, device_policy=device_policy,
+                   pingpong=pingpong)
     ref = _oracle_state(master.numpy())
     hp = oracle_mod.Hparams(lr=lr, weight_decay=wd, max_grad_norm=clip)
     o_t, o_scale, o_good = 0, loss_scale, 0
@@ -416,7 +417,7 @@ def test_host_shard_gradient_accumulation(zero_lib, oracle_mod):
 
 
 def _policy_run(zero_lib, oracle_mod, *, out_of_place, skip, bad_steps, steps, async_steps,
-                N=4, psi=PSI_SMALL, clip=0.0):
+                N=4, psi=PSI_SMALL, clip=0.0, pingpong=False, staging=0):
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     psi_pad = -(-psi // (N * 128)) * (N * 128)
@@ -425,7 +426,7 @@ def _policy_run(zero_lib, oracle_mod, *, out_of_place, skip, bad_steps, steps, a
     opt = ZeroAdam(psi_pad, N, "bf16", skip_on_overflow=skip, max_grad_norm=clip,
                    loss_scale=4096.0, dynamic_loss_scale=True, growth_interval=2,
                    out_of_place=out_of_place, device=dev, master=master.to(dev),
-                   device_policy=True)
+                   device_policy=True, pingpong=pingpong, smem_staging=staging)
     assert not opt.needs_result
     ref = _oracle_state(master.numpy())
     hp = oracle_mod.Hparams(max_grad_norm=clip)
@@ -577,3 +578,90 @@ def test_host_buffer_is_page_locked_and_huge_page_backed():
     buf.close()
     back.close()
     assert buf.tensor is None
+
+
+# ---------------------------------------------------------------------------
+# Ping-pong state sets: the device keeps which of the two out-of-place sets
+# is current, so a skipped step copies nothing.
+
+@pytest.mark.parametrize("staging", [0, 1])
+@pytest.mark.parametrize("N,dtype", [(4, "bf16"), (8, "bf16"), (3, "fp32")])
+def test_pingpong_skip(zero_lib, oracle_mod, N, dtype, staging):
+    """Step 2 overflows and is skipped; the current set must stay current and
+    the later steps continue from it (host-side bookkeeping)."""
+    opt, _ = run_parity(zero_lib, oracle_mod, N=N, psi=PSI_MULTI_SWEEP if N == 8 else PSI_SMALL,
+                        dtype=dtype, steps=4, skip=True, out_of_place=True, bad_step=2,
+                        loss_scale=1024.0, dynamic=True, staging=staging, pingpong=True)
+    # three applied steps flip the set three times
+    assert int(opt.set_mem[0]) == 1 and opt.cur == 1
+
+
+@pytest.mark.parametrize("clip,bucket", [(0.05, 0), (1.0, 400_000)])
+def test_pingpong_two_pass(zero_lib, oracle_mod, clip, bucket):
+    """With clipping the update runs as a second pass after the step-wide
+    decision: it reads the snapshot of the current set, not the flipped word."""
+    run_parity(zero_lib, oracle_mod, N=8, psi=PSI_MULTI_SWEEP, dtype="bf16", steps=4, skip=True,
+               clip=clip, out_of_place=True, bad_step=3, bucket=bucket, loss_scale=4096.0,
+               dynamic=True, pingpong=True)
+
+
+@pytest.mark.parametrize("staging", [0, 1])
+@pytest.mark.parametrize("async_steps", [False, True])
+def test_pingpong_with_device_policy(zero_lib, oracle_mod, staging, async_steps):
+    """t, the loss scale and the current set all kept on the device, steps
+    enqueued back to back; steps 3 and 4 overflow and are skipped."""
+    _policy_run(zero_lib, oracle_mod, out_of_place=True, skip=True, bad_steps={3, 4}, steps=7,
+                async_steps=async_steps, pingpong=True, staging=staging)
+
+
+def test_pingpong_accumulation(zero_lib, oracle_mod):
+    """Micro-batch accumulation with ping-pong sets: the fused last micro-batch
+    reads and writes the sets the snapshot names; the skipped step 2 copies
+    nothing."""
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    dev = torch.device("cuda:0")
+    N, k, psi = 4, 3, PSI_SMALL
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(17)) * 0.02
+    opt = ZeroAdam(psi_pad, N, "bf16", skip_on_overflow=True, bucket_elems=131_072,
+                   loss_scale=256.0, out_of_place=True, device=dev, master=master.to(dev),
+                   micro_batches=k, pingpong=True)
+    ref = _oracle_state(master.numpy())
+    hp = oracle_mod.Hparams()
+    o_t = 0
+    for step in range(1, 5):
+        micro = [_make_grads(N, psi, psi_pad, "bf16", 1e-3 * 256.0, 3000 * step + mb)
+                 for mb in range(k)]
+        if step == 2:
+            micro[2][1][4321] = float("inf")
+        res = opt.step_accumulated([[g.to(dev) for g in mb] for mb in micro])
+        ores = oracle_mod.zero_step_accum([[_np(g) for g in mb] for mb in micro], ref["master"],
+                                          ref["m"], ref["v"], ref["w"], hp, o_t + 1, 256.0, True)
+        compare_result(res, ores)
+        if ores["applied"]:
+            o_t += 1
+        assert opt.t == o_t
+        compare_state(state_to_numpy(opt.state()), ref, exact=True, tag=f"step {step} ")
+    assert o_t == 3 and int(opt.set_mem[0]) == 1
+
+
+def test_pingpong_skip_launches_no_copy(zero_lib):
+    """A skipped ping-pong step launches no restore kernel: the same number of
+    kernels as an applied one, and the current-set word does not move."""
+    from zero_sharded_mixed_04_gb300.optim import ZeroAdam
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, n = 4, 4 * 128 * 512
+    opt = ZeroAdam(n, N, "bf16", skip_on_overflow=True, out_of_place=True, device=dev,
+                   loss_scale=8.0, pingpong=True)
+    good = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(N)]
+    bad = [g.clone() for g in good]
+    bad[2][77] = float("inf")
+    launches = []
+    for grads in (good, bad, good):
+        before = Z.zero_launch_count()
+        opt.step(grads)
+        launches.append(Z.zero_launch_count() - before)
+    assert launches[0] == launches[1] == launches[2]
+    assert opt.t == 2 and int(opt.set_mem[0]) == 0

@@ -87,6 +87,8 @@ FORMS = {
     "fused-out-of-place-skip": dict(out_of_place=True, skip=True),
     "staged-in-place": dict(staging=1),
     "staged-out-of-place-policy": dict(out_of_place=True, skip=True, staging=1, policy=True),
+    "staged-pingpong-policy": dict(out_of_place=True, skip=True, staging=1, policy=True,
+                                   pingpong=True),
     "two-pass-in-place-skip": dict(skip=True),
     "two-pass-clip": dict(clip=1e9, out_of_place=True),
     "buckets": dict(bucket=4096, skip=True, out_of_place=True),
@@ -109,7 +111,7 @@ def test_crafted_columns_match_the_oracle(zero_lib, oracle_mod, form, N, dtype):
                    bucket_elems=f.get("bucket", 0), loss_scale=LOSS_SCALE,
                    out_of_place=f.get("out_of_place", False), device=dev,
                    smem_staging=f.get("staging", 0), micro_batches=k,
-                   device_policy=f.get("policy", False))
+                   device_policy=f.get("policy", False), pingpong=f.get("pingpong", False))
     grads, pat = _crafted_grads(N, psi_pad, dtype, seed=N)
     master, m, v, w = _initial_state(psi_pad, pat, seed=10 + N)
     opt.load_state(master.to(dev), m.to(dev), v.to(dev), w.to(dev))

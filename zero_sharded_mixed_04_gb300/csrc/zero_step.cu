@@ -93,6 +93,8 @@ struct Ctrl {
     zero_step_result result;   // the outcome, when the caller passes no result pointer
     int policy_error;          // device policy: t fell outside the given window
     unsigned int timeout;      // a bounded wait of the staged kernel gave up
+    int cur;                   // ping-pong: the state set this step reads (0 or 1), set
+                               // by the prologue from the caller's word
     Scalars scalars;           // device policy: this step's scalars, set by the prologue
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
@@ -124,6 +126,7 @@ struct StepArgs {
     int32_t stages;      // staged kernel: shared-memory stages
     uint32_t stage_bytes;// staged kernel: bytes of one stage (N gradient chunks + 3 state chunks)
     int32_t test_stall;  // staged kernel: CTA 0 never copies its first tile (tests the bounded waits)
+    int32_t pingpong;    // 1: read the set ctrl->cur names (0 = src_*, 1 = dst_*), write the other
 };
 
 // The step's scalars: from the kernel arguments, or, under a device policy,
@@ -135,6 +138,35 @@ __device__ __forceinline__ Scalars step_scalars(const StepArgs& a) {
 // Under a device policy a step whose t fell outside its window does nothing.
 __device__ __forceinline__ bool policy_off(const StepArgs& a) {
     return a.sdev != nullptr && a.ctrl->policy_error != 0;
+}
+
+// Ping-pong state sets (zero_plan_set_pingpong).  The plan's src_* buffers
+// are set 0 and its dst_* buffers set 1.  A step reads the set the control
+// block names and writes the other, so `sw` (set 1 is the current one) swaps
+// the two roles.  Without ping-pong sw is false: read src_*, write dst_*.
+__device__ __forceinline__ bool sets_swapped(const StepArgs& a) {
+    return a.pingpong != 0 && a.ctrl->cur != 0;
+}
+__device__ __forceinline__ const float* in_master(const StepArgs& a, bool sw) {
+    return sw ? a.dst_master : a.src_master;
+}
+__device__ __forceinline__ const float* in_m(const StepArgs& a, bool sw) {
+    return sw ? a.dst_m : a.src_m;
+}
+__device__ __forceinline__ const float* in_v(const StepArgs& a, bool sw) {
+    return sw ? a.dst_v : a.src_v;
+}
+__device__ __forceinline__ float* out_master(const StepArgs& a, bool sw) {
+    return sw ? const_cast<float*>(a.src_master) : a.dst_master;
+}
+__device__ __forceinline__ float* out_m(const StepArgs& a, bool sw) {
+    return sw ? const_cast<float*>(a.src_m) : a.dst_m;
+}
+__device__ __forceinline__ float* out_v(const StepArgs& a, bool sw) {
+    return sw ? const_cast<float*>(a.src_v) : a.dst_v;
+}
+__device__ __forceinline__ uint16_t* out_w(const StepArgs& a, bool sw) {
+    return sw ? const_cast<uint16_t*>(a.src_w) : a.dst_w;
 }
 
 // ------------------------------------------------------------------ element math
@@ -298,7 +330,7 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 // earlier micro-batches left in gws (the same two roundings the accumulate
 // kernel makes), and is used at once instead of being written back.
 template <int NT, bool kBF16, bool kAccIn, int U>
-__device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s,
+__device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s, bool sw,
                                              const int64_t (&j)[U], unsigned& bad,
                                              double& sumsq) {
     float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
@@ -306,9 +338,9 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s
     // every load of the U groups is issued before any arithmetic
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        load8(a.src_master, j[u], p[u]);
-        load8(a.src_m, j[u], m[u]);
-        load8(a.src_v, j[u], v[u]);
+        load8(in_master(a, sw), j[u], p[u]);
+        load8(in_m(a, sw), j[u], m[u]);
+        load8(in_v(a, sw), j[u], v[u]);
         if constexpr (kAccIn) load8(a.gws, j[u], acc[u]);
     }
 #pragma unroll
@@ -328,10 +360,10 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        store8(a.dst_master, j[u], p[u]);
-        store8(a.dst_m, j[u], m[u]);
-        store8(a.dst_v, j[u], v[u]);
-        store_w8(a.dst_w, j[u], p[u]);
+        store8(out_master(a, sw), j[u], p[u]);
+        store8(out_m(a, sw), j[u], m[u]);
+        store8(out_v(a, sw), j[u], v[u]);
+        store_w8(out_w(a, sw), j[u], p[u]);
     }
 }
 
@@ -345,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
     unsigned bad = 0;
     double sumsq = 0.0;
     const Scalars s = step_scalars(a);
+    const bool sw = sets_swapped(a);
     const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -353,15 +386,15 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
     constexpr bool kPairs = kBF16 || !kAccIn;
     for (; kPairs && q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
-        fused_groups<NT, kBF16, kAccIn, 2>(a, s, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 2>(a, s, sw, j, bad, sumsq);
     }
     for (; !kPairs && q + stride < n8; q += stride) {
         const int64_t j[1] = {a.begin + q * kVec};
-        fused_groups<NT, kBF16, kAccIn, 1>(a, s, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        fused_groups<NT, kBF16, kAccIn, 1>(a, s, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -487,7 +520,7 @@ __device__ __forceinline__ float4 lds_f4(const void* p) {
 // Consumer work on 4 elements: the tile-relative element e (a multiple of 4)
 // of the stage st, flat index j.
 template <int NT, bool kBF16>
-__device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s,
+__device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s, bool sw,
                                              const unsigned char* st, int e, int64_t j,
                                              unsigned& bad, double& sumsq) {
     constexpr uint32_t gbytes = kBF16 ? 2 : 4;
@@ -525,10 +558,10 @@ __device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s
         adam_element(gs, p[q], m[q], v[q], s);
     }
     sumsq += static_cast<double>(sq);
-    __stcs(reinterpret_cast<float4*>(a.dst_master + j), make_float4(p[0], p[1], p[2], p[3]));
-    __stcs(reinterpret_cast<float4*>(a.dst_m + j), make_float4(m[0], m[1], m[2], m[3]));
-    __stcs(reinterpret_cast<float4*>(a.dst_v + j), make_float4(v[0], v[1], v[2], v[3]));
-    __stcs(reinterpret_cast<uint2*>(a.dst_w + j),
+    __stcs(reinterpret_cast<float4*>(out_master(a, sw) + j), make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(reinterpret_cast<float4*>(out_m(a, sw) + j), make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(reinterpret_cast<float4*>(out_v(a, sw) + j), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<uint2*>(out_w(a, sw) + j),
            make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
 }
 
@@ -552,6 +585,7 @@ __global__ void __launch_bounds__(kStagedThreads)
     }
     __syncthreads();
     const Scalars s = step_scalars(a);
+    const bool sw = sets_swapped(a);
     const int64_t range = (policy_off(a) ? 0 : a.n8) * kVec;  // a multiple of 8
     const int64_t ntiles = (range + kTile - 1) / kTile;
     unsigned bad = 0, timed_out = 0;
@@ -580,9 +614,9 @@ __global__ void __launch_bounds__(kStagedThreads)
                               static_cast<const unsigned char*>(a.grads[i]) + (j - a.gbase) * gbytes,
                               gb, &full[st_i], once);
                 unsigned char* state = st + static_cast<size_t>(n_ranks) * kTile * gbytes;
-                bulk_load(state, a.src_master + j, sb, &full[st_i], once);
-                bulk_load(state + kTile * 4, a.src_m + j, sb, &full[st_i], once);
-                bulk_load(state + 2 * kTile * 4, a.src_v + j, sb, &full[st_i], once);
+                bulk_load(state, in_master(a, sw) + j, sb, &full[st_i], once);
+                bulk_load(state + kTile * 4, in_m(a, sw) + j, sb, &full[st_i], once);
+                bulk_load(state + 2 * kTile * 4, in_v(a, sw) + j, sb, &full[st_i], once);
             }
             // Let every copy this thread issued land before the CTA may exit,
             // whichever wait (its own or a consumer's) gave up.  A tile older
@@ -609,7 +643,7 @@ __global__ void __launch_bounds__(kStagedThreads)
             const unsigned char* st = smem + static_cast<size_t>(st_i) * a.stage_bytes;
 #pragma unroll
             for (int e = 4 * c; e < kTile; e += 4 * kStagedConsumers)
-                if (e < len) staged_chunk<NT, kBF16>(a, s, st, e, a.begin + e0 + e, bad, sumsq);
+                if (e < len) staged_chunk<NT, kBF16>(a, s, sw, st, e, a.begin + e0 + e, bad, sumsq);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st_i]);
         }
@@ -743,13 +777,13 @@ __device__ __forceinline__ void copy_state(const StepArgs& a) {
 // gradient, clipped by coef when the step clips.
 template <int U>
 __device__ __forceinline__ void update_groups(const StepArgs& a, const Scalars& s, float coef,
-                                              const int64_t (&j)[U]) {
+                                              bool sw, const int64_t (&j)[U]) {
     float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        load8(a.src_master, j[u], p[u]);
-        load8(a.src_m, j[u], m[u]);
-        load8(a.src_v, j[u], v[u]);
+        load8(in_master(a, sw), j[u], p[u]);
+        load8(in_m(a, sw), j[u], m[u]);
+        load8(in_v(a, sw), j[u], v[u]);
         load8(a.gws, j[u], g[u]);
     }
 #pragma unroll
@@ -762,33 +796,35 @@ __device__ __forceinline__ void update_groups(const StepArgs& a, const Scalars& 
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        store8(a.dst_master, j[u], p[u]);
-        store8(a.dst_m, j[u], m[u]);
-        store8(a.dst_v, j[u], v[u]);
-        store_w8(a.dst_w, j[u], p[u]);
+        store8(out_master(a, sw), j[u], p[u]);
+        store8(out_m(a, sw), j[u], m[u]);
+        store8(out_v(a, sw), j[u], v[u]);
+        store_w8(out_w(a, sw), j[u], p[u]);
     }
 }
 
 // Second pass of the two-pass form: Adam + BF16 all-gather from the
 // workspace's combined gradient, unless the step was skipped.  A skipped
-// out-of-place step copies src to dst instead.  Two groups per thread in
+// out-of-place step copies src to dst instead, except with ping-pong sets,
+// where the current set simply stays current.  Two groups per thread in
 // flight, as in the fused kernel.
 __global__ void __launch_bounds__(kThreads, 2) zero_update_kernel(const __grid_constant__ StepArgs a) {
     allow_next_launch();
     if (a.ctrl->skip) {
-        if (a.dst_master != a.src_master) copy_state(a);
+        if (a.dst_master != a.src_master && !a.pingpong) copy_state(a);
     } else {
         const float coef = a.ctrl->clip_coef;
         const Scalars s = step_scalars(a);
+        const bool sw = sets_swapped(a);
         const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
         int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
         for (; q + stride < a.n8; q += 2 * stride) {
             const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
-            update_groups<2>(a, s, coef, j);
+            update_groups<2>(a, s, coef, sw, j);
         }
         if (q < a.n8) {
             const int64_t j[1] = {a.begin + q * kVec};
-            update_groups<1>(a, s, coef, j);
+            update_groups<1>(a, s, coef, sw, j);
         }
     }
     // A sub-launch chained to the previous one completes only after it: the
@@ -797,7 +833,8 @@ __global__ void __launch_bounds__(kThreads, 2) zero_update_kernel(const __grid_c
 }
 
 // After a one-pass out-of-place step: a skipped step must leave dst equal to
-// src, so copy it; an applied step needs nothing.
+// src, so copy it; an applied step needs nothing.  Not launched with ping-pong
+// sets, where a skipped step leaves the current set current.
 __global__ void __launch_bounds__(kThreads) zero_restore_kernel(const __grid_constant__ StepArgs a) {
     if (a.ctrl->skip) copy_state(a);
 }
@@ -806,7 +843,8 @@ __global__ void __launch_bounds__(kThreads) zero_restore_kernel(const __grid_con
 // norm and clip coefficient, decides the skip, and writes the result.
 __global__ void __launch_bounds__(kFinalizeThreads)
 zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int skip_on_overflow,
-                     zero_step_result* result, zero_device_policy* policy) {
+                     zero_step_result* result, zero_device_policy* policy,
+                     int32_t* current_set) {
     __shared__ double s[kFinalizeThreads];
     double t = 0.0;
     for (int i = threadIdx.x; i < kMaxGrid; i += kFinalizeThreads) t += partials[i];
@@ -840,6 +878,13 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         r.grad_norm = static_cast<float>(norm);
         r.clip_coef = coef;
         *result = r;
+        // ping-pong: an applied step made the other set current.  The step's
+        // own kernels read the snapshot in ctrl->cur, never this word, so a
+        // second pass after this kernel still reads and writes the right sets.
+        if (current_set != nullptr) {
+            if (!skip) *current_set = ctrl->cur ^ 1;
+            __threadfence_system();
+        }
         if (policy != nullptr) {
             // the host-side rule, kept on the device: t counts applied steps;
             // the dynamic scale backs off after an overflow, grows after
@@ -867,13 +912,20 @@ struct PolicyTable {
     float sbc2[ZERO_POLICY_WINDOW];       // sqrt(1 - beta2^t)
 };
 
-// Device policy, start of a step: picks the scalars for t' = policy->t + 1
-// from the host's window, forms the batch-mean factor from the device's loss
-// scale, and leaves them in the control block for the step's kernels.
-__global__ void zero_policy_prologue_kernel(const zero_device_policy* policy, Ctrl* ctrl,
-                                            Scalars base, PolicyTable table, int64_t t_first,
-                                            int32_t t_count, double ranks_times_micro) {
+// Start of a step that keeps state on the device.
+//   - Ping-pong sets: snapshots which set is current into the control block,
+//     where every kernel of the step reads it.
+//   - Device policy: picks the scalars for t' = policy->t + 1 from the host's
+//     window, forms the batch-mean factor from the device's loss scale, and
+//     leaves them in the control block for the step's kernels.
+__global__ void zero_step_prologue_kernel(const zero_device_policy* policy, Ctrl* ctrl,
+                                          Scalars base, PolicyTable table, int64_t t_first,
+                                          int32_t t_count, double ranks_times_micro,
+                                          const int32_t* current_set) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    if (current_set != nullptr)
+        ctrl->cur = *reinterpret_cast<const volatile int32_t*>(current_set) != 0 ? 1 : 0;
+    if (policy == nullptr) return;
     const int64_t idx = policy->t + 1 - t_first;
     Scalars s = base;
     if (idx < 0 || idx >= t_count) {
@@ -1181,6 +1233,7 @@ StepArgs base_args(const zero_plan* p) {
     a.N = p->N;
     a.clip = p->hp.max_grad_norm > 0.0 ? 1 : 0;
     a.gbase = 0;
+    a.pingpong = p->current_set != nullptr ? 1 : 0;
     return a;
 }
 
@@ -1276,7 +1329,7 @@ int plan_begin(zero_plan* p, void* stream) {
     if (cudaMemsetAsync(p->workspace, 0, kGradOffset, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return ZERO_ERR_CUDA;
-    if (p->policy != nullptr) {
+    if (p->policy != nullptr || p->current_set != nullptr) {
         PolicyTable table{};
         zero_adam_hparams hp = p->hp;
         for (int32_t i = 0; i < p->policy_t_count; ++i) {
@@ -1286,10 +1339,11 @@ int plan_begin(zero_plan* p, void* stream) {
             table.sbc2[i] = si.sbc2;
         }
         const Scalars base = make_scalars(&p->hp, p->N, p->loss_scale);
-        zero_policy_prologue_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        zero_step_prologue_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
             static_cast<const zero_device_policy*>(p->policy),
             reinterpret_cast<Ctrl*>(p->workspace), base, table, p->policy_t_first,
-            p->policy_t_count, static_cast<double>(p->N) * micro_batches_of(&p->hp));
+            p->policy_t_count, static_cast<double>(p->N) * micro_batches_of(&p->hp),
+            static_cast<const int32_t*>(p->current_set));
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
     }
@@ -1340,6 +1394,10 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
             if (!device_memory(a.grads[i])) return ZERO_ERR_ARG;
         if (begin == 0 &&
             (!device_memory(p->src_master) || !device_memory(p->src_m) || !device_memory(p->src_v)))
+            return ZERO_ERR_ARG;
+        // with ping-pong sets the copies may read either set
+        if (begin == 0 && p->current_set != nullptr &&
+            (!device_memory(p->dst_master) || !device_memory(p->dst_m) || !device_memory(p->dst_v)))
             return ZERO_ERR_ARG;
         a.test_stall = p->smem_staging == ZERO_STAGING_TMA_TEST_STALL ? 1 : 0;
     } else if (k > 1 && p->micro_batch == k - 1 && !p->two_pass) {
@@ -1396,7 +1454,7 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
 
     zero_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(
         ctrl, a.partials, p->hp.max_grad_norm, p->hp.skip_on_overflow, result_dev,
-        static_cast<zero_device_policy*>(p->policy));
+        static_cast<zero_device_policy*>(p->policy), static_cast<int32_t*>(p->current_set));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
 
@@ -1404,10 +1462,12 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
         // the first update launch waits for the finalize kernel in stream order
         if (!launch_range(zero_update_kernel, device, a, 0, p->psi_pad, stream, false))
             return ZERO_ERR_CUDA;
-    } else if (!p->in_place && (p->hp.skip_on_overflow || p->policy != nullptr ||
-                                p->smem_staging != ZERO_STAGING_REGISTERS)) {
+    } else if (!p->in_place && p->current_set == nullptr &&
+               (p->hp.skip_on_overflow || p->policy != nullptr ||
+                p->smem_staging != ZERO_STAGING_REGISTERS)) {
         // a skipped step (overflow, a t outside the policy's window, a timed-out
-        // staged wait) must leave dst equal to src
+        // staged wait) must leave dst equal to src.  With ping-pong sets the
+        // current set stays current instead, and nothing is copied.
         a.begin = 0;
         a.n8 = p->psi_pad / kVec;
         if (!launch(zero_restore_kernel, device, a, stream)) return ZERO_ERR_CUDA;
@@ -1520,6 +1580,39 @@ extern "C" int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* 
     plan->policy = attr.devicePointer;
     plan->policy_t_first = t_first;
     plan->policy_t_count = t_count;
+    return ZERO_OK;
+}
+
+extern "C" int zero_plan_set_pingpong(zero_plan* plan, int32_t* current_set) {
+    if (plan == nullptr || plan->state != 1 || current_set == nullptr || !aligned(current_set, 4))
+        return ZERO_ERR_ARG;
+    // Both sets are read and written, so the step must be out of place, the
+    // src set complete, and every buffer of both sets disjoint from the rest.
+    if (plan->in_place) return ZERO_ERR_ARG;
+    if (plan->psi_pad > 0) {
+        if (plan->src_w_bf16 == nullptr) return ZERO_ERR_ARG;
+        const uintptr_t n = static_cast<uintptr_t>(plan->psi_pad);
+        Span sp[ZERO_MAX_RANKS + 12];
+        int k = written_spans(plan, sp);
+        auto add = [&](const void* ptr, uintptr_t bytes, bool written) {
+            if (ptr != nullptr)
+                sp[k++] = Span{reinterpret_cast<uintptr_t>(ptr),
+                               reinterpret_cast<uintptr_t>(ptr) + bytes, written};
+        };
+        add(plan->src_master, 4 * n, true);
+        add(plan->src_m, 4 * n, true);
+        add(plan->src_v, 4 * n, true);
+        add(plan->src_w_bf16, 2 * n, true);
+        for (int i = 0; i < plan->N; ++i) add(plan->grads[i], n * grad_elem_bytes(plan->grad_dtype), false);
+        if (!disjoint(sp, k)) return ZERO_ERR_OVERLAP;
+    }
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, current_set) != cudaSuccess ||
+        attr.devicePointer == nullptr) {
+        cudaGetLastError();
+        return ZERO_ERR_ARG;
+    }
+    plan->current_set = attr.devicePointer;
     return ZERO_OK;
 }
 

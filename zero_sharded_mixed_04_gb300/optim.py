@@ -55,6 +55,11 @@ class ZeroAdam:
     ``out_of_place`` keeps two sets of master/m/v/w and calls
     ``zero_step_into`` (the post-step state lands in the other set, which
     then becomes current).  Otherwise ``zero_step`` updates one set in place.
+
+    ``pingpong`` (out of place only) lets the device keep which set is current
+    (``zero_plan_set_pingpong``): a skipped step then leaves the current set
+    current instead of copying it into the other one.  The host learns the
+    current set when it next synchronises (``state()`` does).
     """
 
     def __init__(self, psi_pad: int, N: int, grad_dtype: str = "bf16", *, lr=1e-3, beta1=0.9,
@@ -63,7 +68,9 @@ class ZeroAdam:
                  dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
                  device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0,
                  host_grad_accum: bool = False, device_policy: bool = False,
-                 smem_staging: int = 0):
+                 smem_staging: int = 0, pingpong: bool = False):
+        if pingpong and not out_of_place:
+            raise ValueError("ping-pong state sets need the out-of-place step")
         self.psi_pad, self.N = psi_pad, N
         self.grad_dtype = Z.ZERO_GRAD_BF16 if grad_dtype == "bf16" else Z.ZERO_GRAD_FP32
         self.hp = Z.make_hparams(lr, beta1, beta2, eps, weight_decay, max_grad_norm, 1,
@@ -93,8 +100,9 @@ class ZeroAdam:
         self._grad_accum_buf = None
         self.grad_accum = None
         if host_grad_accum:
-            from .hostmem import HostBuffer
-            self._grad_accum_buf = HostBuffer(psi_pad, torch.float32)
+            from .hostmem import HostBuffer, gpu_numa_node
+            self._grad_accum_buf = HostBuffer(psi_pad, torch.float32,
+                                              numa_node=gpu_numa_node(self.device))
             self.grad_accum = self._grad_accum_buf.tensor
             self.grad_accum.zero_()
         self.ws_bytes = (Z.ZERO_WORKSPACE_CONTROL_BYTES if host_grad_accum else
@@ -117,13 +125,25 @@ class ZeroAdam:
             self._inflight = collections.deque()
         self.result_t = torch.zeros(4, dtype=torch.int32, pin_memory=True)
         self.last = None
+        # pingpong: the device-kept index of the current set, in pinned memory
+        self.pingpong = pingpong
+        self.set_mem = torch.zeros(1, dtype=torch.int32, pin_memory=True) if pingpong else None
 
     # ---------------------------------------------------------------- state
     def state(self) -> dict:
-        """The current master/m/v (FP32) and working weights (BF16 bits as int16)."""
+        """The current master/m/v (FP32) and working weights (BF16 bits as int16).
+        With ping-pong sets this waits for the device, which alone knows which
+        set is current while steps are in flight."""
+        if self.pingpong:
+            torch.cuda.synchronize(self.device)
+            self.cur = int(self.set_mem[0]) & 1
         return self._bufs[self.cur]
 
     def load_state(self, master, m, v, w) -> None:
+        if self.pingpong:
+            torch.cuda.synchronize(self.device)
+            self.set_mem[0] = 0
+            self.cur = 0
         s = self.state()
         s["master"].copy_(master)
         s["m"].copy_(m)
@@ -147,7 +167,7 @@ class ZeroAdam:
         self.hp.step = self.t + 1
         src = self._bufs[self.cur]
         if (api == "plan" or self.grad_accum is not None or self.policy_mem is not None
-                or self.smem_staging):
+                or self.smem_staging or self.pingpong):
             return self._enqueue_plan(grads, src, stream, bucket_events, span_events)
         if self.out_of_place:
             dst = self._bufs[1 - self.cur]
@@ -168,8 +188,21 @@ class ZeroAdam:
         b = self.hp.bucket_elems or self.psi_pad
         return [(b0, min(self.psi_pad, b0 + b)) for b0 in range(0, self.psi_pad, b)]
 
+    def _sets(self):
+        """(src, dst) buffer sets of the next step's plan: with ping-pong sets
+        always set 0 and set 1 (the device picks which one it reads)."""
+        if self.pingpong:
+            return self._bufs[0], self._bufs[1]
+        src = self._bufs[self.cur]
+        return src, (self._bufs[1 - self.cur] if self.out_of_place else src)
+
+    def _after_enqueue(self) -> None:
+        # with ping-pong sets the device flips the current set itself
+        if self.out_of_place and not self.pingpong:
+            self.cur = 1 - self.cur
+
     def _enqueue_plan(self, grads, src, stream, bucket_events, span_events=None) -> int:
-        dst = self._bufs[1 - self.cur] if self.out_of_place else src
+        src, dst = self._sets()
         plan = Z.zero_plan()
         Z.check(Z.zero_plan_init_ex(plan, grads, self.grad_dtype, src["master"], src["m"],
                                     src["v"], src["w"], dst["master"], dst["m"], dst["v"], dst["w"],
@@ -198,8 +231,7 @@ class ZeroAdam:
         self.first_pass_launches = Z.zero_launch_count() - n0
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
         self._note_enqueued(s)
-        if self.out_of_place:
-            self.cur = 1 - self.cur
+        self._after_enqueue()
         return rc
 
     # ---------------------------------------------------------------- accumulation
@@ -217,8 +249,7 @@ class ZeroAdam:
         if len(micro_grads) != k:
             raise ValueError(f"expected {k} micro-batches, got {len(micro_grads)}")
         self.hp.step = self.t + 1
-        src = self._bufs[self.cur]
-        dst = self._bufs[1 - self.cur] if self.out_of_place else src
+        src, dst = self._sets()
         plan = Z.zero_plan()
         Z.check(Z.zero_plan_init_ex(plan, micro_grads[0], self.grad_dtype, src["master"],
                                     src["m"], src["v"], src["w"], dst["master"], dst["m"],
@@ -246,8 +277,7 @@ class ZeroAdam:
         self.first_pass_launches = Z.zero_launch_count() - n0
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, stream), "zero_plan_end")
         self._note_enqueued(s)
-        if self.out_of_place:
-            self.cur = 1 - self.cur
+        self._after_enqueue()
         return rc
 
     def step_accumulated(self, micro_grads, stream=None) -> dict:
@@ -278,8 +308,7 @@ class ZeroAdam:
         reduces bucket k - 1 from the other slot.  A slot is refilled only once
         the bucket that used it has been read."""
         self.hp.step = self.t + 1
-        src = self._bufs[self.cur]
-        dst = self._bufs[1 - self.cur] if self.out_of_place else src
+        src, dst = self._sets()
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         plan = Z.zero_plan()
         Z.check(Z.zero_plan_init_ex(plan, [None] * self.N, self.grad_dtype, src["master"],
@@ -309,11 +338,12 @@ class ZeroAdam:
             freed[k % 2].record(s)
         rc = Z.check(Z.zero_plan_end(plan, self.result_t, s), "zero_plan_end")
         self._note_enqueued(s)
-        if self.out_of_place:
-            self.cur = 1 - self.cur
+        self._after_enqueue()
         return rc
 
     def _apply_policy(self, plan, stream) -> None:
+        if self.pingpong:
+            Z.check(Z.zero_plan_set_pingpong(plan, self.set_mem), "zero_plan_set_pingpong")
         if self.policy_mem is not None:
             t_first, t_count = self._policy_window(stream)
             Z.check(Z.zero_plan_set_device_policy(plan, self.policy_mem, t_first, t_count),

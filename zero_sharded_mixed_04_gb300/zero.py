@@ -88,7 +88,7 @@ class zero_plan(ctypes.Structure):
                 ("state", ctypes.c_int32), ("micro_batch", ctypes.c_int32),
                 ("policy_t_count", ctypes.c_int32), ("policy_t_first", ctypes.c_int64),
                 ("policy", ctypes.c_void_p), ("overlap_buckets", ctypes.c_int32),
-                ("smem_staging", ctypes.c_int32)]
+                ("smem_staging", ctypes.c_int32), ("current_set", ctypes.c_void_p)]
 
 
 class zero_device_policy(ctypes.Structure):
@@ -124,6 +124,8 @@ _lib.zero_plan_init_ex.argtypes = [_PLAN, _P, _i32, _P, _P, _P, _P, _P, _P, _P, 
 _lib.zero_plan_init_ex.restype = ctypes.c_int
 _lib.zero_plan_set_device_policy.argtypes = [_PLAN, _P, _i64, _i32]
 _lib.zero_plan_set_device_policy.restype = ctypes.c_int
+_lib.zero_plan_set_pingpong.argtypes = [_PLAN, _P]
+_lib.zero_plan_set_pingpong.restype = ctypes.c_int
 _lib.zero_plan_begin.argtypes = [_PLAN, _P]
 _lib.zero_plan_begin.restype = ctypes.c_int
 _lib.zero_plan_bucket.argtypes = [_PLAN, _i64, _i64, _P, _P]
@@ -262,6 +264,12 @@ def zero_plan_set_device_policy(plan: zero_plan, policy, t_first: int, t_count: 
     return _lib.zero_plan_set_device_policy(ctypes.byref(plan), _addr(policy), t_first, t_count)
 
 
+def zero_plan_set_pingpong(plan: zero_plan, current_set) -> int:
+    """current_set: the address of a device-addressable int32 (a pinned host
+    tensor or a device tensor) naming the current state set, 0 or 1."""
+    return _lib.zero_plan_set_pingpong(ctypes.byref(plan), _addr(current_set))
+
+
 def zero_plan_begin(plan: zero_plan, stream=None) -> int:
     return _lib.zero_plan_begin(ctypes.byref(plan), _stream(stream))
 
@@ -319,7 +327,7 @@ def exported_symbols() -> list[str]:
     """Names of the C functions this binding expects the library to export."""
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
             "zero_step_into", "zero_plan_init", "zero_plan_init_ex",
-            "zero_plan_set_device_policy", "zero_plan_begin",
+            "zero_plan_set_device_policy", "zero_plan_set_pingpong", "zero_plan_begin",
             "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
             "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes"]
