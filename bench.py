@@ -2,7 +2,7 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload flat1b_n8] [--api plan|step] [--in-place]
-                [--staging tma|registers]
+                [--staging tma|registers] [--pingpong auto|on|off] [--sequence|--no-sequence]
 
 One step is one pass of the whole hot path over one batch of synthetic
 gradients, resident in device memory when the timed region starts:
@@ -15,14 +15,22 @@ gradients, resident in device memory when the timed region starts:
 The default workload is flat1b_n8: 1,000,000,000 parameters, N=8 BF16 ranks,
 25,000,000-element buckets, dynamic loss scale from 65536, skip on overflow.
 It runs out of place (the plan entry points, as zero_step_into), so the skip
-decision needs no second pass.  The one-pass kernel stages every 2048-element
-tile in shared memory with TMA bulk copies (ZERO_STAGING_TMA); --staging
-registers times the kernel that loads straight into registers instead.
+decision needs no second pass, with ping-pong state sets: the device keeps
+which of the two sets is current, so a skipped step copies nothing.  The
+one-pass kernel stages every 2048-element tile in shared memory with TMA bulk
+copies (ZERO_STAGING_TMA); --staging registers times the kernel that loads
+straight into registers instead.
+
+The steady-state steps all reuse step 1's gradients.  For a workload with an
+injected overflow (flat1b_n8) the line also carries `sequence`: the workload's
+own steps as its configuration lists them, fresh gradients each step and the
++inf on step 3, each step timed on its own.
 
 The printed JSON line carries:
   - value: params/s over all GPUs;
   - the dominant kernel's roofline: algorithmic bytes per launch over its
-    CUDA-event duration, against the measured HBM copy peak;
+    CUDA-event duration, against the measured HBM copy peak (and, beside it,
+    the nominal HBM3e bandwidth);
   - the oracle timed on host cores (cpu_baseline);
   - an end-to-end figure: gradients streamed from pinned host memory through
     two device slots, and the result read back to the host;
@@ -53,6 +61,7 @@ sys.path.insert(0, ROOT)
 METRIC = "params/sec and achieved HBM GB/s (fraction of GB300 peak) per fused ZeRO step"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_04_gb300", "csrc", "zero_step.cu")
 # the committed ncu summary of each one-pass kernel on the full flat1b_n8 workload
 PROFILE_SUMMARY = {
@@ -99,6 +108,15 @@ def parse_args(argv=None):
     ap.add_argument("--psi", type=int, default=0,
                     help="reduced parameter count of the same workload (profiling captures "
                          "only; the benchmark line is the full size)")
+    ap.add_argument("--pingpong", choices=["auto", "on", "off"], default="auto",
+                    help="ping-pong state sets (the device keeps which out-of-place set is "
+                         "current, so a skipped step copies nothing); 'auto' uses them for an "
+                         "out-of-place step that can be skipped")
+    seq = ap.add_mutually_exclusive_group()
+    seq.add_argument("--sequence", dest="sequence", action="store_true", default=None,
+                     help="also time the workload's own step sequence (fresh gradients each "
+                          "step, the injected overflow included)")
+    seq.add_argument("--no-sequence", dest="sequence", action="store_false")
     return ap.parse_args(argv)
 
 
@@ -244,18 +262,21 @@ def kernel_source_hash() -> str:
     return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
-def profiled_traffic_per_param(kernel: str) -> float | None:
-    """DRAM bytes per parameter of a one-pass kernel from its committed ncu
-    summary, if it was taken on the kernel source as it is now."""
+def profiled_figures(kernel: str) -> dict | None:
+    """From a one-pass kernel's committed ncu summary, if it was taken on the
+    kernel source as it is now: DRAM bytes per parameter and, when given, the
+    serialised duration of one full-size launch under ncu."""
     try:
         text = open(PROFILE_SUMMARY[kernel]).read()
     except OSError:
         return None
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     b = re.search(r"traffic_bytes_per_param:\s*([0-9.]+)", text)
+    d = re.search(r"ncu_launch_us:\s*([0-9.]+)", text)
     if not h or not b or h.group(1) != kernel_source_hash():
         return None
-    return float(b.group(1))
+    return {"traffic_bytes_per_param": float(b.group(1)),
+            "ncu_launch_us": float(d.group(1)) if d else None}
 
 
 def alg_bytes_per_param(wl) -> int:
@@ -264,28 +285,46 @@ def alg_bytes_per_param(wl) -> int:
 
 
 def cpu_baseline(oracle, wl, grads, master, budget_s: float, max_elems: int) -> dict:
-    """The oracle, single-threaded, on the first elements of the same
-    gradients and master weights (copied from the device), stepped until
-    ``budget_s`` of CPU time is used."""
+    """The oracle on the first elements of the same gradients and master
+    weights (copied from the device), stepped until ``budget_s`` of wall time
+    is used: single-threaded, as it stands (the reported value), and then its
+    OpenMP build on every host core (``all_cores``)."""
     import numpy as np
     from zero_sharded_mixed_04_gb300 import synth
     n = min(max_elems, wl.psi_pad) // (wl.N * 128) * (wl.N * 128)
     g = [synth.to_numpy_grad(x[:n]) for x in grads]
-    p = master[:n].cpu().numpy().copy()
-    m, v, w = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+    p0 = master[:n].cpu().numpy().copy()
     hp = oracle.Hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
                         weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm)
-    steps, t0 = 0, time.process_time()
-    w0 = time.perf_counter()
-    while True:
-        oracle.zero_step(g, p, m, v, w, hp, steps + 1, wl.loss_scale, wl.skip_on_overflow)
-        steps += 1
-        if time.process_time() - t0 >= budget_s:
-            break
-    wall = time.perf_counter() - w0
-    return {"value": steps * n / wall, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{steps} oracle step(s) of {wl.name} on its first {n} parameters "
-                      f"(all {wl.N} ranks), single-threaded C, {wall:.1f} s wall"}
+
+    def timed(parallel: bool, budget: float):
+        p = p0.copy()
+        m, v, w = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+        oracle.zero_step(g, p, m, v, w, hp, 1, wl.loss_scale, wl.skip_on_overflow,
+                         parallel=parallel)   # loads the library, faults the pages in
+        steps, w0 = 0, time.perf_counter()
+        while True:
+            oracle.zero_step(g, p, m, v, w, hp, steps + 2, wl.loss_scale, wl.skip_on_overflow,
+                             parallel=parallel)
+            steps += 1
+            if time.perf_counter() - w0 >= budget:
+                break
+        return steps, time.perf_counter() - w0
+
+    steps, wall = timed(False, budget_s)
+    out = {"value": steps * n / wall, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"{steps} oracle step(s) of {wl.name} on its first {n} parameters "
+                     f"(all {wl.N} ranks), single-threaded C, {wall:.1f} s wall"}
+    try:
+        cores = os.cpu_count() or 1
+        steps_p, wall_p = timed(True, budget_s / 2)
+        out["all_cores"] = {
+            "value": steps_p * n / wall_p, "unit": UNIT, "cores": cores, "kind": "oracle (OpenMP build)",
+            "sample": f"{steps_p} step(s) of the same sample, the oracle's elementwise loops on "
+                      f"{cores} threads, {wall_p:.1f} s wall"}
+    except Exception as exc:  # no OpenMP runtime on this host
+        out["all_cores"] = {"unavailable": str(exc).splitlines()[0]}
+    return out
 
 
 # ------------------------------------------------------------------ our arm
@@ -305,6 +344,8 @@ def run_ours(args, world, rank, local):
     out_of_place = not args.in_place
     device_policy = args.policy == "device" or (
         args.policy == "auto" and (wl.skip_on_overflow or wl.dynamic_loss_scale))
+    pingpong = out_of_place and (args.pingpong == "on" or (
+        args.pingpong == "auto" and wl.skip_on_overflow and not args.host_grad_accum))
     grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
     # the end-to-end leg's pinned host copy of the gradients, made before the
     # large device allocations as an application would hold it from the start
@@ -325,7 +366,7 @@ def run_ours(args, world, rank, local):
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
                    out_of_place=out_of_place, device=dev, master=master,
                    micro_batches=args.micro_batches, host_grad_accum=args.host_grad_accum,
-                   device_policy=device_policy,
+                   device_policy=device_policy, pingpong=pingpong,
                    smem_staging=Z.ZERO_STAGING_TMA if args.staging == "tma" else 0)
     buckets = opt.bucket_bounds()
     k_micro = max(1, args.micro_batches)
@@ -410,13 +451,24 @@ def run_ours(args, world, rank, local):
         # the committed ncu summary covers the fused kernel on the full flat1b_n8
         # workload only
         staged = args.staging == "tma" and not two_pass and k_micro == 1
-        tpp = (profiled_traffic_per_param("zero_fused_staged_kernel" if staged
-                                          else "zero_fused_kernel")
-               if wl.name == "flat1b_n8" and not two_pass and k_micro == 1 else None)
+        prof = (profiled_figures("zero_fused_staged_kernel" if staged else "zero_fused_kernel")
+                if wl.name == "flat1b_n8" and not two_pass and k_micro == 1 else None)
+        traffic = (None if prof is None
+                   else round(prof["traffic_bytes_per_param"] * wl.psi_pad / n_launch))
+        ncu_gbs = (None if prof is None or not prof["ncu_launch_us"]
+                   else round(traffic / (prof["ncu_launch_us"] * 1e-6) / 1e9, 1))
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4),
-                    "traffic": (None if tpp is None else round(tpp * wl.psi_pad / n_launch)),
+                    "traffic": traffic,
                     "peak_kind": peak_kind,
+                    "peak_label": "measured HBM copy" if peak_kind == "measured"
+                                  else "fallback HBM copy",
+                    "nominal_peak": NOMINAL_HBM_GBS,
+                    "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                    # DRAM bytes of one launch over its serialised, cold-cache
+                    # duration under ncu (the committed summary's figures)
+                    "ncu_gbs": ncu_gbs,
+                    "ncu_frac": None if ncu_gbs is None else round(ncu_gbs / peak, 4),
                     "kernel": ("zero_reduce_kernel" if two_pass else
                                "zero_fused_staged_kernel" if staged else "zero_fused_kernel"),
                     "buckets_per_step": len(buckets),
@@ -446,6 +498,11 @@ def run_ours(args, world, rank, local):
                 else k_micro * ng + 8 * k_micro - 4 + 30)
     step_gbs = b_alg * wl.psi_pad / (ms / 1e3) / 1e9
 
+    sequence = None
+    run_seq = args.sequence if args.sequence is not None else bool(wl.inject_inf_step)
+    if run_seq and k_micro == 1 and not args.host_grad_accum:
+        sequence = run_sequence(opt, wl, grads, stream, dev, group, b_alg)
+
     e2e = None
     if e2e_unavailable is not None:
         e2e = {"unavailable": e2e_unavailable}
@@ -470,6 +527,8 @@ def run_ours(args, world, rank, local):
                    "micro_batches": k_micro, "staging": args.staging,
                    "grad_shard": "pinned host memory" if args.host_grad_accum else "HBM",
                    "step_policy": "device" if device_policy else "host",
+                   "state_sets": ("ping-pong (device keeps the current set)" if pingpong else
+                                  "swapped by the host" if out_of_place else "one, in place"),
                    "entry": ("zero_plan_* (= zero_step_into)" if args.api == "plan"
                              else "zero_step_into") if out_of_place else
                    ("zero_plan_* (= zero_step)" if args.api == "plan" else "zero_step"),
@@ -478,7 +537,9 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, N ranks in HBM"},
         "achieved_hbm_gbs": round(step_gbs, 1),
         "hbm_frac": round(step_gbs / peak, 4),
+        "hbm_frac_of_nominal": round(step_gbs / NOMINAL_HBM_GBS, 4),
         "roofline": roofline,
+        "sequence": sequence,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -489,14 +550,58 @@ def run_ours(args, world, rank, local):
     group.close()
 
 
+def run_sequence(opt, wl, grads, stream, dev, group, b_alg) -> dict:
+    """The workload's own steps as its configuration lists them: fresh seeded
+    gradients every step, drawn at the loss scale that step uses, and the
+    injected +inf on its step, which must be skipped.  Each step is timed on
+    its own by CUDA events around its launches; the gradients are drawn
+    between the timed regions.  Steps are enqueued as the timed steps are
+    (with a device policy, back to back with no host read); the outcome is
+    checked against the workload's script at the end."""
+    import torch
+    from zero_sharded_mixed_04_gb300 import synth
+    opt.finish_pending()
+    t0, scale = opt.t, opt.scaler.scale
+    evs = []
+    for step in range(1, wl.steps + 1):
+        synth.make_grads(wl, step, dev, loss_scale=scale, out=grads)
+        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        e[0].record(stream)
+        res = opt.step_async(grads, stream)
+        e[1].record(stream)
+        evs.append(e)
+        overflow = step == wl.inject_inf_step
+        if res is not None and res["applied"] == overflow:
+            raise RuntimeError(f"sequence step {step}: expected it {'skipped' if overflow else 'applied'}")
+        if overflow and wl.dynamic_loss_scale:
+            scale *= 0.5   # the scale the next step's gradients carry
+    opt.finish_pending()
+    skipped = [s for s in range(1, wl.steps + 1) if s == wl.inject_inf_step]
+    if opt.t != t0 + wl.steps - len(skipped) or (wl.dynamic_loss_scale and opt.scaler.scale != scale):
+        raise RuntimeError("the step sequence did not skip exactly its injected step")
+    ms = [group.max(a.elapsed_time(b)) for a, b in evs]
+    applied_ms = [m for s, m in enumerate(ms, 1) if s not in skipped]
+    mean = sum(ms) / len(ms)
+    return {"steps": wl.steps, "skipped_steps": skipped, "ms": [round(m, 4) for m in ms],
+            "applied_ms_mean": round(sum(applied_ms) / len(applied_ms), 4),
+            "skipped_ms": round(ms[skipped[0] - 1], 4) if skipped else None,
+            "mean_ms": round(mean, 4),
+            "value": round(group.sum(float(wl.psi)) / (mean / 1e3), 1), "unit": UNIT,
+            "achieved_hbm_gbs": round(b_alg * wl.psi_pad / (mean / 1e3) / 1e9, 1),
+            "gradients": "fresh seeded draws per step, at the step's loss scale; "
+                         "the injected +inf on its step"}
+
+
 def pin_host_grads(grads):
     """The gradients in one page-locked host buffer backed by huge pages
-    (hostmem.HostBuffer), every rank's a slice of it."""
-    from zero_sharded_mixed_04_gb300.hostmem import HostBuffer
+    (hostmem.HostBuffer), every rank's a slice of it, placed on the host
+    memory node next to the GPU."""
+    from zero_sharded_mixed_04_gb300.hostmem import HostBuffer, gpu_numa_node
     n = grads[0].numel()
     # every rank on this node allocates one such buffer at about the same time
     ranks_here = int(os.environ.get("LOCAL_WORLD_SIZE", os.environ.get("WORLD_SIZE", "1")))
-    buf = HostBuffer(n * len(grads), grads[0].dtype, share=ranks_here)
+    buf = HostBuffer(n * len(grads), grads[0].dtype, share=ranks_here,
+                     numa_node=gpu_numa_node(grads[0].device))
     host = [buf.tensor[i * n:(i + 1) * n] for i in range(len(grads))]
     for h, g in zip(host, grads):
         h.copy_(g)
@@ -551,7 +656,8 @@ def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
     link_gbs = h2d / link_s / 1e9
     dt = group.max(statistics.median(times))
     mean = group.max(sum(times) / len(times))
-    kind = buf.kind
+    from zero_sharded_mixed_04_gb300.hostmem import cpu_nodes
+    kind, numa_node, numa_placed = buf.kind, buf.numa_node, buf.numa_placed
     del host, slots, host_grads
     torch.cuda.synchronize(dev)
     buf.close()
@@ -563,6 +669,11 @@ def run_e2e(args, opt, grads, host_grads, wl, stream, dev, group) -> dict:
             "h2d_link_gbs": round(link_gbs, 1),
             "h2d_copies_only_ms": round(link_s * 1e3, 3),
             "host_buffer": kind,
+            "host_numa_node": numa_node,
+            "host_pages_on_node": numa_placed,
+            "host_cpu_nodes": len(cpu_nodes()),
+            "weights_d2h": "none: the BF16 working weights stay on the device for the next "
+                           "forward pass; the host reads the 16-byte step result",
             "path": "pinned host grads -> two device bucket slots -> zero_plan_bucket; "
                     "result read by the host"}
 
