@@ -29,6 +29,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "zero_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libzero_oracle.so")
+# the same source built with OpenMP: the all-cores timing mode (CPU baseline only)
+_LIB_OMP_PATH = os.path.join(_HERE, "libzero_oracle_omp.so")
 _CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 BF16 = 0
@@ -37,17 +39,20 @@ PAD_UNIT = 128
 
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle's C source into a shared library next to it."""
-    stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+def build(force: bool = False, parallel: bool = False) -> str:
+    """Compile the oracle's C source into a shared library next to it
+    (``parallel``: the OpenMP build of the same source)."""
+    path = _LIB_OMP_PATH if parallel else _LIB_PATH
+    stale = not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC)
     if force or stale:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+        tmp = path + f".tmp{os.getpid()}"
+        extra = ["-fopenmp"] if parallel else []
+        subprocess.run(["gcc", *_CFLAGS, *extra, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, path)
+    return path
 
 
 class _Hparams(ctypes.Structure):
@@ -68,48 +73,55 @@ class _Result(ctypes.Structure):
                 ("clip_coef", ctypes.c_float)]
 
 
-def _load():
-    global _lib
+def _declare(lib):
+    P = ctypes.c_void_p
+    i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+    lib.orc_f32_to_bf16_array.argtypes = [P, P, i64]
+    lib.orc_f32_to_bf16.argtypes = [f32]
+    lib.orc_f32_to_bf16.restype = ctypes.c_uint16
+    lib.orc_layout.argtypes = [P, i64, i32, P, P, P, P]
+    lib.orc_layout.restype = i32
+    lib.orc_ledger_bytes.argtypes = [i64, i32, i32, i32, i32]
+    lib.orc_ledger_bytes.restype = i64
+    lib.orc_comm_volume.argtypes = [i64, i32, i32, i32]
+    lib.orc_comm_volume.restype = i64
+    lib.orc_step_scalars.argtypes = [P, i32, i32, f64, P]
+    lib.orc_reduce_scatter.argtypes = [P, i32, i32, i64, i32, f32, P]
+    lib.orc_all_reduce.argtypes = [P, i32, i32, i64, f32, P]
+    lib.orc_all_gather_f32.argtypes = [P, i32, i64, P]
+    lib.orc_zero_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
+    lib.orc_zero_step.restype = i32
+    lib.orc_ddp_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
+    lib.orc_ddp_step.restype = i32
+    lib.orc_zero_step_accum.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, i32, f64,
+                                         i32, P]
+    lib.orc_zero_step_accum.restype = i32
+    lib.orc_gather_range.argtypes = [P, i32, i64, i64, i64, P]
+    lib.orc_gather_range.restype = i32
+    lib.orc_zero3_peak_bytes.argtypes = [P, i64, i32, i32, i32]
+    lib.orc_zero3_peak_bytes.restype = i64
+    lib.orc_check_accumulate.argtypes = [P, i32, i32, i64, f32, P, P]
+    lib.orc_step_window.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64,
+                                    i32, i32, f32]
+    lib.orc_clip_coef_from_sumsq.argtypes = [f64, f64]
+    lib.orc_clip_coef_from_sumsq.restype = f32
+    lib.orc_loss_scale_update.argtypes = [P, P, i32, i32, f64, f64]
+    return lib
+
+
+def _load(parallel: bool = False):
+    global _lib, _lib_omp
     with _lock:
+        if parallel:
+            if _lib_omp is None:
+                _lib_omp = _declare(ctypes.CDLL(build(parallel=True)))
+            return _lib_omp
         if _lib is None:
             # ORACLE_LIB_OVERRIDE loads another build of the oracle's source;
             # only the mutation test uses it, to check that the pins catch
             # planted mistakes
             override = os.environ.get("ORACLE_LIB_OVERRIDE")
-            lib = ctypes.CDLL(override if override else build())
-            P = ctypes.c_void_p
-            i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
-            lib.orc_f32_to_bf16_array.argtypes = [P, P, i64]
-            lib.orc_f32_to_bf16.argtypes = [f32]
-            lib.orc_f32_to_bf16.restype = ctypes.c_uint16
-            lib.orc_layout.argtypes = [P, i64, i32, P, P, P, P]
-            lib.orc_layout.restype = i32
-            lib.orc_ledger_bytes.argtypes = [i64, i32, i32, i32, i32]
-            lib.orc_ledger_bytes.restype = i64
-            lib.orc_comm_volume.argtypes = [i64, i32, i32, i32]
-            lib.orc_comm_volume.restype = i64
-            lib.orc_step_scalars.argtypes = [P, i32, i32, f64, P]
-            lib.orc_reduce_scatter.argtypes = [P, i32, i32, i64, i32, f32, P]
-            lib.orc_all_reduce.argtypes = [P, i32, i32, i64, f32, P]
-            lib.orc_all_gather_f32.argtypes = [P, i32, i64, P]
-            lib.orc_zero_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
-            lib.orc_zero_step.restype = i32
-            lib.orc_ddp_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
-            lib.orc_ddp_step.restype = i32
-            lib.orc_zero_step_accum.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, i32, f64,
-                                                 i32, P]
-            lib.orc_zero_step_accum.restype = i32
-            lib.orc_gather_range.argtypes = [P, i32, i64, i64, i64, P]
-            lib.orc_gather_range.restype = i32
-            lib.orc_zero3_peak_bytes.argtypes = [P, i64, i32, i32, i32]
-            lib.orc_zero3_peak_bytes.restype = i64
-            lib.orc_check_accumulate.argtypes = [P, i32, i32, i64, f32, P, P]
-            lib.orc_step_window.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64,
-                                            i32, i32, f32]
-            lib.orc_clip_coef_from_sumsq.argtypes = [f64, f64]
-            lib.orc_clip_coef_from_sumsq.restype = f32
-            lib.orc_loss_scale_update.argtypes = [P, P, i32, i32, f64, f64]
-            _lib = lib
+            _lib = _declare(ctypes.CDLL(override if override else build()))
     return _lib
 
 
@@ -258,13 +270,15 @@ def _result(r: _Result) -> dict:
 
 
 def zero_step(grads, master, m, v, w, hp: Hparams, t: int, loss_scale: float = 1.0,
-              skip_on_overflow: bool = False) -> dict:
+              skip_on_overflow: bool = False, parallel: bool = False) -> dict:
     """One ZeRO step (owner form) in place on flat master/m/v (float32) and w
-    (BF16 bits, uint16), all of psi_pad elements; grads is a list of N arrays."""
+    (BF16 bits, uint16), all of psi_pad elements; grads is a list of N arrays.
+    ``parallel`` runs the OpenMP build (the CPU baseline's all-cores mode):
+    the same elements, the norm in fixed-order per-thread partials."""
     N = len(grads)
     res = _Result()
     c = hp._c()
-    rc = _load().orc_zero_step(_ptr_array(grads), _grad_dtype(grads), N, master.size,
+    rc = _load(parallel).orc_zero_step(_ptr_array(grads), _grad_dtype(grads), N, master.size,
                                _ptr(master), _ptr(m), _ptr(v), _ptr(w), ctypes.byref(c), t,
                                loss_scale, int(skip_on_overflow), ctypes.byref(res))
     if rc != 0:

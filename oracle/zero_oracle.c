@@ -37,11 +37,23 @@
  *     the quiet NaN 0x7FC0.
  *   - The flat vector is padded with zeros to a multiple of N*128 elements
  *     and owner r holds the contiguous slice [r*S, (r+1)*S), S = psi_pad/N.
+ *
+ * All-cores timing mode.  Built with -fopenmp, the elementwise loops of the
+ * whole-vector step run on all host cores; every element is computed exactly
+ * as in the single-thread build.  The step-wide sum of squares is then formed
+ * as one FP64 partial per contiguous chunk of the vector (one chunk per
+ * thread), each summed in element order, and the partials are added in chunk
+ * order: a fixed order for a given thread count.  With one chunk (the
+ * single-thread build) it is the sequential sum.  Only the benchmark's CPU
+ * baseline uses that build; every pin and parity check uses the plain one.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_BF16 0
 #define ORC_FP32 1
@@ -329,6 +341,7 @@ void orc_reduce_scatter(const void* const* grads, int32_t dtype, int32_t N,
                         int64_t psi_pad, int32_t r, float inv, float* out_shard)
 {
     int64_t shard = psi_pad / N;
+#pragma omp parallel for schedule(static)
     for (int64_t j = 0; j < shard; ++j)
         out_shard[j] = orc_reduce_element(grads, dtype, N, (int64_t)r * shard + j, inv);
 }
@@ -353,6 +366,44 @@ void orc_all_gather_f32(const float* const* shards, int32_t N, int64_t shard,
 /* ------------------------------------------------------------------------ */
 /* The whole step                                                             */
 /* ------------------------------------------------------------------------ */
+
+/* Step-wide overflow flag and sum of squares of g[0..n): one FP64 partial per
+ * contiguous chunk, each summed in element order, added in chunk order.  The
+ * single-thread build has one chunk, i.e. the plain sequential sum. */
+static void orc_check_vector(const float* g, int64_t n, int32_t* bad, double* sumsq)
+{
+    int chunks = 1;
+#ifdef _OPENMP
+    chunks = omp_get_max_threads();
+    if (chunks < 1)
+        chunks = 1;
+#endif
+    double partial[256];
+    int32_t flag[256];
+    if (chunks > 256)
+        chunks = 256;
+#pragma omp parallel for schedule(static, 1) num_threads(chunks)
+    for (int c = 0; c < chunks; ++c) {
+        int64_t lo = n * c / chunks, hi = n * (c + 1) / chunks;
+        double s = 0.0;
+        int32_t b = 0;
+        for (int64_t j = lo; j < hi; ++j) {
+            if (!orc_is_finite(g[j]))
+                b = 1;
+            s = s + (double)g[j] * (double)g[j];
+        }
+        partial[c] = s;
+        flag[c] = b;
+    }
+    double total = 0.0;
+    int32_t any = 0;
+    for (int c = 0; c < chunks; ++c) {
+        total = total + partial[c];
+        any = any | flag[c];
+    }
+    *bad = any;
+    *sumsq = total;
+}
 
 typedef struct {
     int32_t applied;          /* 1 = state updated, 0 = skipped            */
@@ -390,11 +441,7 @@ int orc_zero_step(const void* const* grads, int32_t dtype, int32_t N, int64_t ps
     /* step-wide overflow check and sum of squares, over every owner's slice */
     int32_t bad = 0;
     double sumsq = 0.0;
-    for (int64_t j = 0; j < psi_pad; ++j) {
-        if (!orc_is_finite(g[j]))
-            bad = 1;
-        sumsq = sumsq + (double)g[j] * (double)g[j];
-    }
+    orc_check_vector(g, psi_pad, &bad, &sumsq);
     res->found_nonfinite = bad;
     res->sumsq = sumsq;
     res->grad_norm = (float)sqrt(sumsq);
@@ -406,17 +453,23 @@ int orc_zero_step(const void* const* grads, int32_t dtype, int32_t N, int64_t ps
     }
     if (hp->max_grad_norm > 0.0) {
         res->clip_coef = orc_clip_coef(hp->max_grad_norm, sqrt(sumsq));
+#pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < psi_pad; ++j)
             g[j] = g[j] * res->clip_coef;
     }
     /* each owner updates its own slice */
-    for (int32_t r = 0; r < N; ++r)
-        for (int64_t j = (int64_t)r * shard; j < (int64_t)(r + 1) * shard; ++j)
+    for (int32_t r = 0; r < N; ++r) {
+        int64_t lo = (int64_t)r * shard, hi = (int64_t)(r + 1) * shard;
+#pragma omp parallel for schedule(static)
+        for (int64_t j = lo; j < hi; ++j)
             orc_adam_element(g[j], &master[j], &m[j], &v[j], &s);
+    }
     /* all-gather of the owners' BF16 slices into the full view */
-    for (int32_t r = 0; r < N; ++r)
+    for (int32_t r = 0; r < N; ++r) {
+#pragma omp parallel for schedule(static)
         for (int64_t j = 0; j < shard; ++j)
             w[(int64_t)r * shard + j] = orc_f32_to_bf16(master[(int64_t)r * shard + j]);
+    }
     res->applied = 1;
     free(g);
     return 0;
