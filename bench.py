@@ -62,7 +62,9 @@ METRIC = "params/sec and achieved HBM GB/s (fraction of GB300 peak) per fused Ze
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
-KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_04_gb300", "csrc", "zero_step.cu")
+# the step kernels' code: the profile summaries are tied to a hash of these
+KERNEL_SOURCES = [os.path.join(ROOT, "zero_sharded_mixed_04_gb300", "csrc", f)
+                  for f in ("zero_step.cu", "zero_elem.cuh", "zero_common.cuh")]
 # the committed ncu summary of each one-pass kernel on the full flat1b_n8 workload
 PROFILE_SUMMARY = {
     "zero_fused_kernel": os.path.join(ROOT, "profiles", "zero_fused_kernel_flat1b_n8.md"),
@@ -251,11 +253,14 @@ def read_peaks() -> tuple[float, str]:
 
 
 def kernel_source_hash() -> str:
-    """sha256 (first 16 hex digits) of the kernel source's code: comments,
-    trailing spaces and blank lines removed, so that a comment edit does not
-    void the profiles taken on the same code."""
-    with open(KERNEL_SOURCE) as f:
-        text = f.read()
+    """sha256 (first 16 hex digits) of the step kernels' code (the kernel file
+    and the headers it includes, in that order): comments, trailing spaces and
+    blank lines removed, so that a comment edit does not void the profiles
+    taken on the same code."""
+    text = ""
+    for path in KERNEL_SOURCES:
+        with open(path) as f:
+            text += f.read() + "\n"
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     lines = [re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines()]
     code = "\n".join(line for line in lines if line)

@@ -76,8 +76,11 @@ typedef enum {
     ZERO_ERR_OVERLAP = -6,    /* two buffers that must be disjoint overlap         */
     ZERO_ERR_TOO_LARGE = -7,  /* the step needs more scratch than zero_step_noalloc's
                                  fixed array holds                                 */
-    ZERO_ERR_POLICY_WINDOW = -8 /* device policy: the step's t fell outside the window
+    ZERO_ERR_POLICY_WINDOW = -8, /* device policy: the step's t fell outside the window
                                  of bias corrections it was given; nothing changed  */
+    ZERO_ERR_BOUNDS = -9      /* debug build only: a kernel found an index outside a
+                                 buffer, skipped that access and did not apply the
+                                 step (see zero_debug_bounds_violations)            */
 } zero_status;
 
 typedef enum {
@@ -118,8 +121,8 @@ typedef struct {
 
 /* Outcome of one step, written by the device at the end of the step. */
 typedef struct {
-    int32_t status;           /* ZERO_OK (applied), ZERO_STEP_SKIPPED, ZERO_ERR_TIMEOUT or
-                                 ZERO_ERR_POLICY_WINDOW                              */
+    int32_t status;           /* ZERO_OK (applied), ZERO_STEP_SKIPPED, ZERO_ERR_TIMEOUT,
+                                 ZERO_ERR_POLICY_WINDOW or (debug build) ZERO_ERR_BOUNDS */
     uint32_t found_nonfinite; /* 1 if any combined gradient element was inf or NaN        */
     float grad_norm;          /* L2 norm of the combined batch-mean gradient, before clip */
     float clip_coef;          /* factor applied to the gradient (1 without clipping)      */
@@ -530,6 +533,21 @@ const char* zero_status_str(int status);
 /* Number of kernels this library has launched in this process.  Host only,
  * monotonic, thread-safe.  Memsets and copies are not counted. */
 uint64_t zero_launch_count(void);
+
+/* Debug build.  The same sources compiled with -DZERO_DEBUG give
+ * libzero_gb300_debug.so, with the same entry points.  There every kernel
+ * checks each index range it is about to touch against the lengths of the
+ * buffers involved (the state arrays, the gradient buffers or staging slots,
+ * the workspace, the shards and the view of a gather).  An access outside
+ * them is not made: the kernel skips it and counts it, and a step that saw one
+ * ends with status ZERO_ERR_BOUNDS and is not applied: t does not advance, out
+ * of place dst is restored from src (with ping-pong sets the current set stays
+ * current), and in place the elements reached before may already be updated.
+ * No check traps or asserts, so the device stays usable.
+ * Returns the number of skipped out-of-range accesses counted on the current
+ * device since the previous call, and resets the count; -1 in the release
+ * build, which has no checks.  Host only; waits for the device. */
+int64_t zero_debug_bounds_violations(void);
 
 /* ------------------------------------------------------------------------
  * zero_step without a caller-provided workspace.  The pages have no

@@ -358,3 +358,17 @@ def test_pingpong_argument_checks(zero_lib):
     # not once ping-pong makes it an output too
     p = plan_of([grads[1], 2 * GB, 3 * GB, 4 * GB], dst)
     assert Z.zero_plan_set_pingpong(p, word) == Z.ZERO_ERR_OVERLAP
+
+
+def test_release_build_has_no_bounds_checks(zero_lib):
+    """The release library reports -1 (no checks compiled in) without any CUDA
+    call; the debug library exports the same entry points."""
+    import ctypes as C
+    from zero_sharded_mixed_04_gb300 import build
+    if zero_lib.DEBUG_BUILD:
+        pytest.skip("the binding loaded the debug build")
+    assert zero_lib.zero_debug_bounds_violations() == -1
+    if os.path.exists(build.DEBUG_LIB_PATH):
+        dbg = C.CDLL(build.DEBUG_LIB_PATH)
+        for name in _declared_functions():
+            assert hasattr(dbg, name), f"{name} missing from the debug build"

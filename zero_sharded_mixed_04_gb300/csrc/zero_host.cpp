@@ -107,6 +107,7 @@ extern "C" const char* zero_status_str(int status) {
         case ZERO_ERR_TIMEOUT: return "bounded wait inside a kernel timed out";
         case ZERO_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
         case ZERO_ERR_OVERLAP: return "buffers that must be disjoint overlap";
+        case ZERO_ERR_BOUNDS: return "index outside a buffer (debug build): access skipped";
         case ZERO_ERR_POLICY_WINDOW:
             return "device policy: the step's t fell outside its window of bias corrections";
         case ZERO_ERR_TOO_LARGE:

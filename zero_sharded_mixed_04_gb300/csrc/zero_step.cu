@@ -39,29 +39,18 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
 #include <utility>
 
-#include <nvtx3/nvToolsExt.h>
-
+#include "zero_common.cuh"
+#include "zero_elem.cuh"
 #include "zero_gb300.h"
 
 namespace {
 
-// NVTX range around a host entry point, so that profilers show which step,
-// bucket or gather enqueued the kernels that follow it.  Without a profiler
-// attached this costs a check of one pointer.
-struct NvtxRange {
-    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
-    ~NvtxRange() { nvtxRangePop(); }
-    NvtxRange(const NvtxRange&) = delete;
-    NvtxRange& operator=(const NvtxRange&) = delete;
-};
-
-constexpr int kThreads = 256;             // threads per CTA of the streaming kernels
-constexpr int kVec = 8;                   // elements per thread per group (16 B of BF16)
 constexpr int kMaxGrid = 2048;            // CTAs per launch, at most
 constexpr int kFinalizeThreads = 1024;
 constexpr int kMaxWarps = 32;             // finish_cta's per-warp slots: blocks of <= 1024 threads
@@ -69,19 +58,6 @@ constexpr size_t kCtrlBytes = 256;
 constexpr size_t kPartialsOffset = kCtrlBytes;
 constexpr size_t kGradOffset = kPartialsOffset + kMaxGrid * sizeof(double);  // 256-B aligned
 
-std::atomic<uint64_t> g_launches{0};
-
-// Per-step FP32 scalars, each rounded once from FP64.
-struct Scalars {
-    float inv;        // 1 / (N * loss_scale)
-    float b1, omb1;   // beta1, 1 - beta1
-    float b2, omb2;   // beta2, 1 - beta2
-    float eps;
-    float step_size;  // lr / (1 - beta1^t)
-    float sbc2;       // sqrt(1 - beta2^t)
-    float decay;      // 1 - lr * weight_decay
-    int use_decay;
-};
 
 // Control block at the start of the workspace.  It is zeroed at the start of
 // every step.
@@ -95,6 +71,7 @@ struct Ctrl {
     unsigned int timeout;      // a bounded wait of the staged kernel gave up
     int cur;                   // ping-pong: the state set this step reads (0 or 1), set
                                // by the prologue from the caller's word
+    unsigned int bounds;       // debug build: a kernel skipped an out-of-range access
     Scalars scalars;           // device policy: this step's scalars, set by the prologue
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
@@ -127,6 +104,9 @@ struct StepArgs {
     uint32_t stage_bytes;// staged kernel: bytes of one stage (N gradient chunks + 3 state chunks)
     int32_t test_stall;  // staged kernel: CTA 0 never copies its first tile (tests the bounded waits)
     int32_t pingpong;    // 1: read the set ctrl->cur names (0 = src_*, 1 = dst_*), write the other
+    int64_t limit;       // elements in every state array and in the workspace gradient (psi_pad)
+    int64_t grad_lo;     // flat elements [grad_lo, grad_hi) that the grads[i] buffers hold
+    int64_t grad_hi;
 };
 
 // The step's scalars: from the kernel arguments, or, under a device policy,
@@ -139,6 +119,44 @@ __device__ __forceinline__ Scalars step_scalars(const StepArgs& a) {
 __device__ __forceinline__ bool policy_off(const StepArgs& a) {
     return a.sdev != nullptr && a.ctrl->policy_error != 0;
 }
+
+#ifdef ZERO_DEBUG
+constexpr bool kDebugBuild = true;
+#else
+constexpr bool kDebugBuild = false;
+#endif
+
+// Debug build (-DZERO_DEBUG): before touching elements [j, j + len) a kernel
+// checks them against the lengths of the buffers involved: the state arrays
+// and the workspace gradient hold [0, limit), the gradient buffers (or the
+// staging slot) [grad_lo, grad_hi).  An access outside is skipped, counted,
+// and makes the step end with ZERO_ERR_BOUNDS; nothing traps.  The release
+// build compiles every check to `true`.
+#ifdef ZERO_DEBUG
+__device__ unsigned long long g_step_bounds_violations;
+
+__device__ __forceinline__ bool range_inside(const StepArgs& a, int64_t j, int64_t len,
+                                             bool grads) {
+    bool ok = j >= 0 && len >= 0 && j + len <= a.limit;
+    if (grads) ok = ok && j >= a.grad_lo && j + len <= a.grad_hi;
+    return ok;
+}
+__device__ __forceinline__ void record_violation(const StepArgs& a) {
+    atomicOr(&a.ctrl->bounds, 1u);
+    atomicAdd(&g_step_bounds_violations, 1ull);
+}
+__device__ __forceinline__ bool range_ok(const StepArgs& a, int64_t j, int64_t len, bool grads) {
+    const bool ok = range_inside(a, j, len, grads);
+    if (!ok) record_violation(a);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool range_inside(const StepArgs&, int64_t, int64_t, bool) {
+    return true;
+}
+__device__ __forceinline__ void record_violation(const StepArgs&) {}
+__device__ __forceinline__ bool range_ok(const StepArgs&, int64_t, int64_t, bool) { return true; }
+#endif
 
 // Ping-pong state sets (zero_plan_set_pingpong).  The plan's src_* buffers
 // are set 0 and its dst_* buffers set 1.  A step reads the set the control
@@ -168,74 +186,6 @@ __device__ __forceinline__ float* out_v(const StepArgs& a, bool sw) {
 __device__ __forceinline__ uint16_t* out_w(const StepArgs& a, bool sw) {
     return sw ? const_cast<uint16_t*>(a.src_w) : a.dst_w;
 }
-
-// ------------------------------------------------------------------ element math
-
-__device__ __forceinline__ bool is_nonfinite(float x) {
-    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
-}
-
-// BF16 is the top half of an FP32 word; element 2q of a 16-byte vector is the
-// low half of 32-bit word q.
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest, ties to even
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Owner update of one element: AdamW with bias correction, every operator
-// rounded to FP32 on its own.
-__device__ __forceinline__ void adam_element(float g, float& p, float& m, float& v,
-                                             const Scalars& s) {
-    if (s.use_decay) p = __fmul_rn(p, s.decay);
-    m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
-    v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
-    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sbc2), s.eps);
-    p = __fsub_rn(p, __fmul_rn(s.step_size, __fdiv_rn(m, den)));
-}
-
-// ------------------------------------------------------------------ vector loads
-//
-// Global memory only: __ldcs / __stcs are the global-space cache-streaming
-// forms (ld.global.cs / st.global.cs).  Shared-memory stages are read with
-// lds_u2 / lds_f4 below.
-
-template <bool kBF16>
-struct GradVec;
-
-template <>
-struct GradVec<true> {
-    uint4 r;
-    __device__ __forceinline__ void load(const void* base, int64_t j) {
-        r = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + j));
-    }
-    __device__ __forceinline__ void add_to(float (&g)[kVec]) const {
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            g[2 * q] = __fadd_rn(g[2 * q], bf16_lo(w[q]));
-            g[2 * q + 1] = __fadd_rn(g[2 * q + 1], bf16_hi(w[q]));
-        }
-    }
-};
-
-template <>
-struct GradVec<false> {
-    float4 a, b;
-    __device__ __forceinline__ void load(const void* base, int64_t j) {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + j);
-        a = __ldcs(p);
-        b = __ldcs(p + 1);
-    }
-    __device__ __forceinline__ void add_to(float (&g)[kVec]) const {
-        g[0] = __fadd_rn(g[0], a.x); g[1] = __fadd_rn(g[1], a.y);
-        g[2] = __fadd_rn(g[2], a.z); g[3] = __fadd_rn(g[3], a.w);
-        g[4] = __fadd_rn(g[4], b.x); g[5] = __fadd_rn(g[5], b.y);
-        g[6] = __fadd_rn(g[6], b.z); g[7] = __fadd_rn(g[7], b.w);
-    }
-};
 
 // The reduce-scatter of one 8-element group: every rank's contribution to
 // these same elements, added in rank order starting from +0.  NT > 0 fixes N
@@ -267,38 +217,6 @@ __device__ __forceinline__ void combine(const StepArgs& a, int64_t j, float (&g)
     }
 }
 
-__device__ __forceinline__ void load8(const float* base, int64_t j, float (&x)[kVec]) {
-    const float4* p = reinterpret_cast<const float4*>(base + j);
-    const float4 u = __ldcs(p), w = __ldcs(p + 1);
-    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
-    x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
-}
-
-__device__ __forceinline__ void store8(float* base, int64_t j, const float (&x)[kVec]) {
-    float4* p = reinterpret_cast<float4*>(base + j);
-    __stcs(p, make_float4(x[0], x[1], x[2], x[3]));
-    __stcs(p + 1, make_float4(x[4], x[5], x[6], x[7]));
-}
-
-__device__ __forceinline__ void store_w8(uint16_t* base, int64_t j, const float (&p)[kVec]) {
-    const uint4 packed = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                                    pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
-    __stcs(reinterpret_cast<uint4*>(base + j), packed);
-}
-
-// Programmatic dependent launch.  Consecutive bucket launches of one step
-// touch disjoint elements, so launch k+1 may start streaming while launch k
-// drains.  Every CTA allows the next launch to be scheduled as soon as it
-// starts.  The one write that needs ordering (the CTA's norm slot) waits for
-// the previous grid to complete.  The next grid's CTAs can only be scheduled
-// once every CTA of this grid is resident, so that wait always ends.
-__device__ __forceinline__ void allow_next_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 // End of a CTA's share: publish the overflow flag (one atomic per warp that
 // saw a non-finite value) and add the CTA's sum of squares to its FP64 slot.
 // Warp-shuffle tree, then the warps in order, so the sum is deterministic.
@@ -318,7 +236,10 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
         // previous launch's: wait for that grid to complete first.  Without a
         // programmatic launch this returns at once.
         grid_dependency_wait();
-        a.partials[blockIdx.x] += t;
+        if (blockIdx.x < kMaxGrid)
+            a.partials[blockIdx.x] += t;
+        else
+            record_violation(a);
     }
 }
 
@@ -386,15 +307,17 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
     constexpr bool kPairs = kBF16 || !kAccIn;
     for (; kPairs && q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+        if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
         fused_groups<NT, kBF16, kAccIn, 2>(a, s, sw, j, bad, sumsq);
     }
     for (; !kPairs && q + stride < n8; q += stride) {
         const int64_t j[1] = {a.begin + q * kVec};
+        if (!range_ok(a, j[0], kVec, true)) continue;
         fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
+        if (range_ok(a, j[0], kVec, true)) fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -605,6 +528,12 @@ __global__ void __launch_bounds__(kStagedThreads)
                 const int64_t e0 = t * kTile;
                 const int64_t len = (range - e0 < kTile) ? range - e0 : kTile;
                 const int64_t j = a.begin + e0;
+                if (!range_ok(a, j, len, true)) {
+                    // a tile outside the buffers: complete the stage's phase
+                    // without copying, and the consumers skip it too
+                    mbar_arrive(&full[st_i]);
+                    continue;
+                }
                 unsigned char* st = smem + static_cast<size_t>(st_i) * a.stage_bytes;
                 const uint32_t gb = static_cast<uint32_t>(len) * gbytes;
                 const uint32_t sb = static_cast<uint32_t>(len) * 4u;
@@ -641,9 +570,12 @@ __global__ void __launch_bounds__(kStagedThreads)
             const int64_t e0 = t * kTile;
             const int64_t len = (range - e0 < kTile) ? range - e0 : kTile;
             const unsigned char* st = smem + static_cast<size_t>(st_i) * a.stage_bytes;
+            if (range_inside(a, a.begin + e0, len, true)) {  // as the producer decided
 #pragma unroll
-            for (int e = 4 * c; e < kTile; e += 4 * kStagedConsumers)
-                if (e < len) staged_chunk<NT, kBF16>(a, s, sw, st, e, a.begin + e0 + e, bad, sumsq);
+                for (int e = 4 * c; e < kTile; e += 4 * kStagedConsumers)
+                    if (e < len)
+                        staged_chunk<NT, kBF16>(a, s, sw, st, e, a.begin + e0 + e, bad, sumsq);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st_i]);
         }
@@ -689,11 +621,12 @@ __global__ void __launch_bounds__(kThreads, 2) zero_reduce_kernel(const __grid_c
     int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     for (; q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+        if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
         reduce_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        reduce_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
+        if (range_ok(a, j[0], kVec, true)) reduce_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
     }
     finish_cta(a, bad, sumsq);
 }
@@ -747,11 +680,12 @@ __global__ void __launch_bounds__(kThreads, 2) zero_accum_kernel(const __grid_co
     int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     for (; q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+        if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
         accum_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        accum_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
+        if (range_ok(a, j[0], kVec, true)) accum_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
     }
     finish_cta(a, a.acc_last ? bad : 0u, sumsq);
 }
@@ -761,6 +695,7 @@ __device__ __forceinline__ void copy_state(const StepArgs& a) {
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; q < a.n8;
          q += stride) {
         const int64_t j = a.begin + q * kVec;
+        if (!range_ok(a, j, kVec, false)) continue;
         float x[kVec];
         load8(a.src_master, j, x);
         store8(a.dst_master, j, x);
@@ -820,11 +755,12 @@ __global__ void __launch_bounds__(kThreads, 2) zero_update_kernel(const __grid_c
         int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
         for (; q + stride < a.n8; q += 2 * stride) {
             const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+            if (!range_ok(a, j[0], kVec, false) || !range_ok(a, j[1], kVec, false)) continue;
             update_groups<2>(a, s, coef, sw, j);
         }
         if (q < a.n8) {
             const int64_t j[1] = {a.begin + q * kVec};
-            update_groups<1>(a, s, coef, sw, j);
+            if (range_ok(a, j[0], kVec, false)) update_groups<1>(a, s, coef, sw, j);
         }
     }
     // A sub-launch chained to the previous one completes only after it: the
@@ -860,7 +796,8 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         const int nonfinite = ctrl->nonfinite != 0u;
         const int window_miss = (policy != nullptr && ctrl->policy_error) ? 1 : 0;
         const int timeout = ctrl->timeout != 0u;
-        const int skip = ((skip_on_overflow && nonfinite) || window_miss || timeout) ? 1 : 0;
+        const int bounds = ctrl->bounds != 0u;   // debug build only
+        const int skip = ((skip_on_overflow && nonfinite) || window_miss || timeout || bounds) ? 1 : 0;
         float coef = 1.0f;
         if (max_norm > 0.0 && !skip) {
             const double c = max_norm / (norm + 1e-6);
@@ -870,7 +807,8 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
         ctrl->clip_coef = coef;
         ctrl->grad_norm = static_cast<float>(norm);
         zero_step_result r;
-        r.status = timeout       ? ZERO_ERR_TIMEOUT
+        r.status = bounds        ? ZERO_ERR_BOUNDS
+                   : timeout     ? ZERO_ERR_TIMEOUT
                    : window_miss ? ZERO_ERR_POLICY_WINDOW
                    : skip        ? ZERO_STEP_SKIPPED
                                  : ZERO_OK;
@@ -889,7 +827,7 @@ zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int sk
             // the host-side rule, kept on the device: t counts applied steps;
             // the dynamic scale backs off after an overflow, grows after
             // growth_interval clean steps
-            if (!window_miss && !timeout) {
+            if (!window_miss && !timeout && !bounds) {
                 if (!skip) policy->t += 1;
                 if (policy->growth_interval > 0) {
                     if (nonfinite) {
@@ -975,34 +913,6 @@ StepKernel pick(int N, bool bf16) {
     }
 }
 
-// CTAs per SM for a kernel on a device with the given dynamic shared memory,
-// measured once and cached.
-int resident_ctas(const void* fn, int device, int threads, size_t smem = 0) {
-    static std::mutex mu;
-    static std::map<std::tuple<const void*, int, size_t>, int> cache;
-    std::lock_guard<std::mutex> lock(mu);
-    auto key = std::make_tuple(fn, device, smem);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1)
-        n = 1;
-    cache[key] = n;
-    return n;
-}
-
-int sm_count(int device) {
-    static std::mutex mu;
-    static std::map<int, int> cache;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(device);
-    if (it != cache.end()) return it->second;
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
-        n = 1;
-    cache[device] = n;
-    return n;
-}
 
 // Launch shape of a step kernel: the register kernels take one 8-element group
 // per thread and no dynamic shared memory; the staged kernel one kTile tile
@@ -1065,7 +975,8 @@ constexpr int64_t kLaunchAlignGroups = 32;  // 256 elements
 // kernel before it on the stream only if overlap_first; the others always
 // follow a sub-launch of the same range.
 bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t end,
-                  cudaStream_t stream, bool overlap_first, const Shape& sh = Shape{}) {
+                  cudaStream_t stream, bool overlap_first, const Shape& sh = Shape{},
+                  int64_t overrun_groups = 0) {
     const int64_t groups = (end - begin) / kVec;
     if (groups <= 0) return true;
     const int64_t parts = (groups * kVec + kLaunchElems - 1) / kLaunchElems;
@@ -1079,12 +990,12 @@ bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t 
     for (int64_t k = 0, g0 = 0; g0 < groups; ++k, g0 += per) {
         a.begin = begin + g0 * kVec;
         a.n8 = (groups - g0 < per) ? groups - g0 : per;
+        if (g0 + per >= groups) a.n8 += overrun_groups;  // the last launch (debug tests only)
         if (!launch(fn, device, a, stream, k > 0 || overlap_first, sh)) return false;
     }
     return true;
 }
 
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The staged kernel's TMA copies read device memory only (not pinned host or
 // managed memory, which the register kernels can also read).
@@ -1213,6 +1124,23 @@ int written_spans(const zero_plan* p, Span* out) {
     return k;
 }
 
+// Debug builds only, to test the checks: ZERO_DEBUG_TEST_OVERRUN=g makes the
+// last launch of each pass over the vector cover g more 8-element groups past
+// its end (at most 1024), which the kernels' checks must skip.  The release
+// build never overruns.
+int64_t debug_test_overrun() {
+#ifdef ZERO_DEBUG
+    static const int64_t g = [] {
+        const char* v = std::getenv("ZERO_DEBUG_TEST_OVERRUN");
+        const long long x = v != nullptr ? std::atoll(v) : 0;
+        return static_cast<int64_t>(x < 0 ? 0 : (x > 1024 ? 1024 : x));
+    }();
+    return g;
+#else
+    return 0;
+#endif
+}
+
 StepArgs base_args(const zero_plan* p) {
     char* ws = static_cast<char*>(p->workspace);
     StepArgs a{};
@@ -1234,6 +1162,9 @@ StepArgs base_args(const zero_plan* p) {
     a.clip = p->hp.max_grad_norm > 0.0 ? 1 : 0;
     a.gbase = 0;
     a.pingpong = p->current_set != nullptr ? 1 : 0;
+    a.limit = p->psi_pad;
+    a.grad_lo = 0;
+    a.grad_hi = p->psi_pad;
     return a;
 }
 
@@ -1375,6 +1306,8 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
             a.grads[i] = bucket_grads[i];
         }
         a.gbase = begin;
+        a.grad_lo = begin;   // a staging slot holds this bucket only
+        a.grad_hi = end;
     } else {
         for (int i = 0; i < p->N; ++i)
             if (p->grads[i] == nullptr) return ZERO_ERR_ARG;
@@ -1418,7 +1351,8 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     // 0.  The first bucket of a pass (begin == 0) never overlaps: when
     // accumulating it reads what the previous micro-batch wrote.
     const bool overlap = p->overlap_buckets != 0 && begin > 0;
-    if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap, shape))
+    if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap, shape,
+                      end == p->psi_pad ? debug_test_overrun() : 0))
         return ZERO_ERR_CUDA;
     p->cursor = end;
     // accumulating: a micro-batch that covered the vector hands over to the
@@ -1460,16 +1394,18 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
 
     if (p->two_pass) {
         // the first update launch waits for the finalize kernel in stream order
-        if (!launch_range(zero_update_kernel, device, a, 0, p->psi_pad, stream, false))
+        if (!launch_range(zero_update_kernel, device, a, 0, p->psi_pad, stream, false, Shape{},
+                          debug_test_overrun()))
             return ZERO_ERR_CUDA;
     } else if (!p->in_place && p->current_set == nullptr &&
                (p->hp.skip_on_overflow || p->policy != nullptr ||
-                p->smem_staging != ZERO_STAGING_REGISTERS)) {
+                p->smem_staging != ZERO_STAGING_REGISTERS || kDebugBuild)) {
         // a skipped step (overflow, a t outside the policy's window, a timed-out
-        // staged wait) must leave dst equal to src.  With ping-pong sets the
-        // current set stays current instead, and nothing is copied.
+        // staged wait, or in a debug build an access the checks skipped) must
+        // leave dst equal to src.  With ping-pong sets the current set stays
+        // current instead, and nothing is copied.
         a.begin = 0;
-        a.n8 = p->psi_pad / kVec;
+        a.n8 = p->psi_pad / kVec + debug_test_overrun();
         if (!launch(zero_restore_kernel, device, a, stream)) return ZERO_ERR_CUDA;
     }
     p->state = 1;
@@ -1627,156 +1563,25 @@ extern "C" int zero_plan_end(zero_plan* plan, zero_step_result* result, void* st
     return plan_end(plan, result, stream);
 }
 
+namespace zero_internal {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace zero_internal
+
 extern "C" uint64_t zero_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-// ------------------------------------------------------------------ ZeRO-3 layer gather
-//
-// The full view of a layer, assembled from the owners' BF16 shards: the
-// all-gather before a layer runs under ZeRO-3.  Pure data movement: 2 B read
-// and 2 B written per element.
-
-namespace {
-
-struct GatherArgs {
-    const uint16_t* shards[ZERO_MAX_RANKS];
-    uint16_t* view;
-    int64_t shard;  // elements per shard (a multiple of kVec)
-    int64_t begin;  // first element of the range in the full view
-    int64_t n;      // elements in the range
-    // The range cut at shard boundaries (vector path): segment s copies
-    // seg_len[s] elements from shard seg_shard[s] at seg_src[s] to the view at
-    // seg_dst[s].  At most one segment per shard.
-    int64_t seg_src[ZERO_MAX_RANKS];
-    int64_t seg_dst[ZERO_MAX_RANKS];
-    int64_t seg_len[ZERO_MAX_RANKS];
-    int32_t seg_shard[ZERO_MAX_RANKS];
-    int32_t segments;
-    int32_t wait_previous;  // 0 under ZERO3_GATHER_OVERLAP_PREVIOUS
-};
-
-// 16-byte vectors in flight per thread, and CTAs of kThreads per SM at most.
-// Measured as CUDA-graph replays of the two-view pass: 2 and 6 gave 0.090 ms
-// per GPT-2-small pass and 0.666 ms per pass of twenty 50M-element layers,
-// against 0.097 and 0.671 ms with 4 vectors and every resident CTA (6 per SM);
-// 1, 4 and 8 vectors with 2 to 8 CTAs per SM were no better.
-constexpr int kGatherUnroll = 2;
-constexpr int kGatherCtasPerSm = 6;
-
-// The gathers are launched as programmatic dependents of whatever precedes
-// them on the stream, so their CTAs are scheduled while that kernel drains.
-// Unless the caller declared that kernel independent of this gather
-// (ZERO3_GATHER_OVERLAP_PREVIOUS), every thread waits for it to complete
-// before its first access, which keeps the plain stream order.
-__device__ __forceinline__ void gather_prologue(const GatherArgs& g) {
-    allow_next_launch();
-    if (g.wait_previous) grid_dependency_wait();
-}
-
-// begin is a multiple of kVec, so every segment is a whole number of 8-element
-// groups on both sides; the last segment may end with n % 8 single elements.
-__global__ void __launch_bounds__(kThreads) zero3_gather_vec_kernel(const __grid_constant__ GatherArgs g) {
-    gather_prologue(g);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    for (int s = 0; s < g.segments; ++s) {
-        const uint4* src = reinterpret_cast<const uint4*>(g.shards[g.seg_shard[s]] + g.seg_src[s]);
-        uint4* dst = reinterpret_cast<uint4*>(g.view + g.seg_dst[s]);
-        const int64_t n8 = g.seg_len[s] / kVec;
-        int64_t q = tid;
-        for (; q + (kGatherUnroll - 1) * stride < n8; q += kGatherUnroll * stride) {
-            uint4 x[kGatherUnroll];
-#pragma unroll
-            for (int u = 0; u < kGatherUnroll; ++u) x[u] = __ldcs(src + q + u * stride);
-#pragma unroll
-            for (int u = 0; u < kGatherUnroll; ++u) __stcs(dst + q + u * stride, x[u]);
-        }
-        for (; q < n8; q += stride) __stcs(dst + q, __ldcs(src + q));
-        const int64_t tail = g.seg_len[s] - n8 * kVec;  // only the last segment has one
-        if (tid < tail) {
-            const int64_t i = n8 * kVec + tid;
-            g.view[g.seg_dst[s] + i] = g.shards[g.seg_shard[s]][g.seg_src[s] + i];
-        }
-    }
-}
-
-// Any begin: element by element (a layer that starts at an odd offset).
-__global__ void __launch_bounds__(kThreads) zero3_gather_elem_kernel(const __grid_constant__ GatherArgs g) {
-    gather_prologue(g);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < g.n; i += stride) {
-        const int64_t j = g.begin + i;
-        const int64_t r = j / g.shard;
-        g.view[i] = g.shards[r][j - r * g.shard];
-    }
-}
-
-}  // namespace
-
-extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t shard, int64_t begin,
-                            int64_t end, uint16_t* view, uint32_t flags, void* stream) {
-    NvtxRange range("zero3_gather");
-    if (shards == nullptr || N < 1 || N > ZERO_MAX_RANKS || shard < 0 || shard % kVec != 0 ||
-        begin < 0 || end < begin || end > static_cast<int64_t>(N) * shard ||
-        (flags & ~ZERO3_GATHER_OVERLAP_PREVIOUS) != 0)
-        return ZERO_ERR_ARG;
-    const int64_t n = end - begin;
-    if (n == 0) return ZERO_OK;
-    if (view == nullptr) return ZERO_ERR_ARG;
-    if (!aligned(view, ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
-    GatherArgs g{};
-    const uintptr_t vlo = reinterpret_cast<uintptr_t>(view), vhi = vlo + 2 * static_cast<uintptr_t>(n);
-    for (int i = 0; i < N; ++i) {
-        if (shards[i] == nullptr) return ZERO_ERR_ARG;
-        if (!aligned(shards[i], ZERO_ALIGN_BYTES)) return ZERO_ERR_ALIGN;
-        const uintptr_t lo = reinterpret_cast<uintptr_t>(shards[i]);
-        const uintptr_t hi = lo + 2 * static_cast<uintptr_t>(shard);
-        if (lo < vhi && vlo < hi) return ZERO_ERR_OVERLAP;
-        g.shards[i] = shards[i];
-    }
-    g.view = view;
-    g.shard = shard;
-    g.begin = begin;
-    g.n = n;
-    g.wait_previous = (flags & ZERO3_GATHER_OVERLAP_PREVIOUS) ? 0 : 1;
-    // cut [begin, end) at shard boundaries
-    g.segments = 0;
-    for (int64_t at = begin; at < end;) {
-        const int64_t r = at / shard;
-        const int64_t stop = (end < (r + 1) * shard) ? end : (r + 1) * shard;
-        g.seg_shard[g.segments] = static_cast<int32_t>(r);
-        g.seg_src[g.segments] = at - r * shard;
-        g.seg_dst[g.segments] = at - begin;
-        g.seg_len[g.segments] = stop - at;
-        ++g.segments;
-        at = stop;
-    }
-    int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess) return ZERO_ERR_CUDA;
-    const bool vec = begin % kVec == 0;
-    const void* fn = vec ? reinterpret_cast<const void*>(zero3_gather_vec_kernel)
-                         : reinterpret_cast<const void*>(zero3_gather_elem_kernel);
-    const int64_t units = vec ? (n + kVec * kGatherUnroll - 1) / (kVec * kGatherUnroll) : n;
-    const int64_t full = static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, kThreads);
-    int64_t grid = (units + kThreads - 1) / kThreads;
-    if (grid > full) grid = full;
-    const int64_t cap = static_cast<int64_t>(kGatherCtasPerSm) * sm_count(device);
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t err = vec ? cudaLaunchKernelEx(&cfg, zero3_gather_vec_kernel, g)
-                                : cudaLaunchKernelEx(&cfg, zero3_gather_elem_kernel, g);
-    if (err != cudaSuccess) return ZERO_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA;
+extern "C" int64_t zero_debug_bounds_violations(void) {
+#ifdef ZERO_DEBUG
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    unsigned long long n = 0;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyFromSymbol(&n, g_step_bounds_violations, sizeof n) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_step_bounds_violations, &zero, sizeof zero) != cudaSuccess)
+        return -1;
+    const int64_t g = zero_internal::gather_bounds_violations_take();
+    return g < 0 ? -1 : static_cast<int64_t>(n) + g;
+#else
+    return -1;
+#endif
 }
 
 // ------------------------------------------------------------------ no-allocation entry point

@@ -16,7 +16,9 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libzero_gb300.so")
+# ZERO_GB300_DEBUG=1 loads the debug build (device-side bounds checks) instead
+DEBUG_BUILD = os.environ.get("ZERO_GB300_DEBUG", "") not in ("", "0")
+LIB_PATH = os.path.join(_PKG, "libzero_gb300_debug.so" if DEBUG_BUILD else "libzero_gb300.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -40,6 +42,7 @@ ZERO_ERR_WORKSPACE = -5
 ZERO_ERR_OVERLAP = -6
 ZERO_ERR_TOO_LARGE = -7
 ZERO_ERR_POLICY_WINDOW = -8
+ZERO_ERR_BOUNDS = -9
 ZERO_POLICY_WINDOW = 16
 
 ZERO_WORKSPACE_CONTROL_BYTES = 16640
@@ -147,6 +150,8 @@ _lib.zero_status_str.argtypes = [ctypes.c_int]
 _lib.zero_status_str.restype = ctypes.c_char_p
 _lib.zero_launch_count.argtypes = []
 _lib.zero_launch_count.restype = ctypes.c_uint64
+_lib.zero_debug_bounds_violations.argtypes = []
+_lib.zero_debug_bounds_violations.restype = ctypes.c_int64
 
 
 class ZeroError(RuntimeError):
@@ -323,6 +328,12 @@ def zero_launch_count() -> int:
     return _lib.zero_launch_count()
 
 
+def zero_debug_bounds_violations() -> int:
+    """Out-of-range accesses the debug build's kernels skipped since the last
+    call (and resets the count); -1 for the release build."""
+    return _lib.zero_debug_bounds_violations()
+
+
 def exported_symbols() -> list[str]:
     """Names of the C functions this binding expects the library to export."""
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
@@ -330,4 +341,5 @@ def exported_symbols() -> list[str]:
             "zero_plan_set_device_policy", "zero_plan_set_pingpong", "zero_plan_begin",
             "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
-            "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes"]
+            "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes",
+            "zero_debug_bounds_violations"]
