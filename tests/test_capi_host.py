@@ -372,3 +372,27 @@ def test_release_build_has_no_bounds_checks(zero_lib):
         dbg = C.CDLL(build.DEBUG_LIB_PATH)
         for name in _declared_functions():
             assert hasattr(dbg, name), f"{name} missing from the debug build"
+
+
+@pytest.mark.parametrize("which", ["ragged6b", "gpt2small"])
+@pytest.mark.parametrize("N", [4, 8])
+def test_layout_of_the_workload_tensor_lists(zero_lib, oracle_mod, which, N):
+    """The C-ABI layout of the workloads' own tensor lists: the ragged
+    6,000,000,007-parameter list (about 90 tensors of 1 to 2^27 elements) and
+    GPT-2-small's, against the oracle's layout, offsets and shard ranges."""
+    from zero_sharded_mixed_04_gb300 import synth
+    sizes = (synth.ragged6b_tensor_sizes() if which == "ragged6b"
+             else synth.gpt2_small_tensor_sizes())
+    rc, lay, offs = zero_lib.zero_init_layout(sizes, N)
+    assert rc == zero_lib.ZERO_OK
+    o_offs, psi, psi_pad, shard = oracle_mod.layout(sizes, N)
+    assert (lay.psi, lay.psi_pad, lay.shard, lay.n_tensors) == (psi, psi_pad, shard, len(sizes))
+    assert list(offs) == list(o_offs)
+    if which == "ragged6b":
+        assert psi == 6_000_000_007 and 1 in sizes and (1 << 27) in sizes
+        assert psi_pad % (N * 128) == 0 and psi_pad - psi < N * 128
+    else:
+        assert psi == 123_588_864
+    for r in range(N):
+        rc, b, e = zero_lib.zero_shard_range(lay, r)
+        assert rc == 0 and (b, e) == (r * shard, (r + 1) * shard)
