@@ -105,8 +105,14 @@ def parse_args(argv=None):
                          "over the workload's layers instead of the step")
     ap.add_argument("--zero3-layer-elems", type=int, default=50_000_000,
                     help="layer size for flat workloads in --zero3-gather")
+    ap.add_argument("--zero3-side-streams", type=int, choices=[1, 2], default=2,
+                    help="--zero3-gather: gather on one side stream (each gather chained to the "
+                         "previous) or on one per view (neighbouring layers concurrent)")
     ap.add_argument("--bucket-elems", type=int, default=-1,
                     help="override the workload's bucket size (0: one bucket, the whole vector)")
+    ap.add_argument("--ranks", type=int, default=0,
+                    help="override the workload's rank count N (for instance k*N, to time one "
+                         "pass over every micro-batch's gradients held at once)")
     ap.add_argument("--psi", type=int, default=0,
                     help="reduced parameter count of the same workload (profiling captures "
                          "only; the benchmark line is the full size)")
@@ -132,6 +138,8 @@ def select_workload(args):
     if args.bucket_elems >= 0:
         wl = dataclasses.replace(wl, name=f"{wl.name}[bucket={args.bucket_elems}]",
                                  bucket_elems=args.bucket_elems)
+    if args.ranks:
+        wl = dataclasses.replace(wl, name=f"{wl.name}[N={args.ranks}]", N=args.ranks)
     return wl
 
 
@@ -772,7 +780,8 @@ def run_zero3_gather(args, world, rank, local):
     torch.cuda.empty_cache()
     w = opt.state()["w"]
     S = lay.shard
-    views = Zero3Views([w[r * S:(r + 1) * S] for r in range(wl.N)], S, layers, device=dev)
+    views = Zero3Views([w[r * S:(r + 1) * S] for r in range(wl.N)], S, layers, device=dev,
+                       side_streams=args.zero3_side_streams)
     stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -802,7 +811,7 @@ def run_zero3_gather(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_pass": round(ms, 4),
             "higher_is_better": True,
             "config": {"workload": wl.name, "N": wl.N, "layers": len(layers),
-                       "largest_layer": max(numel)},
+                       "largest_layer": max(numel), "side_streams": args.zero3_side_streams},
             "achieved_gbs": round(gbs, 1), "peak": peak, "peak_kind": peak_kind,
             "frac": round(gbs / peak, 4),
             "eager": {"ms_per_pass": round(ms_eager, 4),

@@ -9,6 +9,8 @@
   step and gather.
 * The same schedule captured as a CUDA graph and replayed twice over
   different shard contents.
+Both schedules run with one side stream (each gather chained to the one
+before) and with two (neighbouring layers' gathers concurrent).
 """
 from __future__ import annotations
 
@@ -42,7 +44,8 @@ def test_gather_ranges(zero_lib, oracle_mod, N, shard):
         assert (got[e - b:] == 0xFFFF).all(), "wrote past the range"
 
 
-def test_two_view_schedule_after_a_step(zero_lib, oracle_mod):
+@pytest.mark.parametrize("side_streams", [1, 2])
+def test_two_view_schedule_after_a_step(zero_lib, oracle_mod, side_streams):
     from zero_sharded_mixed_04_gb300 import synth
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam, Zero3Views
     dev = torch.device("cuda:0")
@@ -73,7 +76,7 @@ def test_two_view_schedule_after_a_step(zero_lib, oracle_mod):
     def use(i, view):
         got[i] = view.clone()
 
-    Zero3Views(shards, S, layers, device=dev).run(use)
+    Zero3Views(shards, S, layers, device=dev, side_streams=side_streams).run(use)
     torch.cuda.synchronize()
     ref = {"master": master.numpy().copy(), "m": np.zeros(psi_pad, np.float32),
            "v": np.zeros(psi_pad, np.float32), "w": np.zeros(psi_pad, np.uint16)}
@@ -86,7 +89,8 @@ def test_two_view_schedule_after_a_step(zero_lib, oracle_mod):
         assert np.array_equal(got[i].cpu().numpy().view(np.uint16), want), f"layer {i}"
 
 
-def test_two_view_schedule_as_a_cuda_graph(zero_lib, oracle_mod):
+@pytest.mark.parametrize("side_streams", [1, 2])
+def test_two_view_schedule_as_a_cuda_graph(zero_lib, oracle_mod, side_streams):
     """The two-view pass captured once and replayed: each replay gathers what
     the shards hold at that moment, like the eager pass."""
     from zero_sharded_mixed_04_gb300 import synth
@@ -107,7 +111,7 @@ def test_two_view_schedule_as_a_cuda_graph(zero_lib, oracle_mod):
     def use(i, view):
         outs[i].copy_(view)
 
-    views = Zero3Views(shards, S, layers, device=dev)
+    views = Zero3Views(shards, S, layers, device=dev, side_streams=side_streams)
     graph = views.capture(use)
     for seed in (41, 42):
         host = torch.randint(-32768, 32767, (lay.psi_pad,), dtype=torch.int16,

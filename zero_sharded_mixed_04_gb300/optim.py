@@ -470,9 +470,18 @@ class Zero3Views:
     after the layer that held it ran (released).  The layers are flat ranges
     [begin, end) of the vector whose BF16 shards are ``shards`` (N device
     buffers of ``shard`` elements, e.g. the owners' slices of a step's
-    working weights)."""
+    working weights).
 
-    def __init__(self, shards, shard: int, layers, device="cuda"):
+    ``side_streams``: 1 gathers every layer on one side stream, each gather
+    chained to the one before it; 2 gives each view its own side stream, so
+    the gathers of neighbouring layers (which fill different views) may run at
+    the same time, while a view is still refilled only after its previous
+    layer ran.  Either way at most two layers are gathered at once, so the
+    peak ledger (zero3_peak_bytes) holds."""
+
+    def __init__(self, shards, shard: int, layers, device="cuda", side_streams: int = 2):
+        if side_streams not in (1, 2):
+            raise ValueError("side_streams is 1 or 2")
         self.shards = list(shards)
         self.N = len(self.shards)
         self.shard = shard
@@ -481,25 +490,32 @@ class Zero3Views:
         most = max((e - b for b, e in self.layers), default=0)
         self.views = [torch.empty(max(most, 1), dtype=torch.int16, device=self.device)
                       for _ in range(2)]
-        self.side = torch.cuda.Stream(self.device)
+        first = torch.cuda.Stream(self.device)
+        self.sides = [first, torch.cuda.Stream(self.device) if side_streams == 2 else first]
+        self.side = first
         self.gathered = [torch.cuda.Event(), torch.cuda.Event()]
         self.released = [torch.cuda.Event(), torch.cuda.Event()]
 
     def _gather(self, i: int) -> None:
         b, e = self.layers[i]
         slot = i % 2
+        side = self.sides[slot]
         if i >= 2:
             # layers 0 and 1 refill views that the previous pass released
-            # before this pass began; the side stream's wait for the caller's
+            # before this pass began; the side streams' wait for the caller's
             # stream at the start of the pass already orders them
-            self.side.wait_event(self.released[slot])
-        # after the first layer of a pass, the kernel before this gather on the
-        # side stream is the previous layer's gather: it reads the shards and
-        # writes the other view, so this one may start while it drains
-        flags = Z.ZERO3_GATHER_OVERLAP_PREVIOUS if i >= 1 else 0
+            side.wait_event(self.released[slot])
+        # One side stream: after the first layer of a pass the kernel before
+        # this gather is the previous layer's gather, which reads the shards
+        # and writes the other view, so this one may start while it drains.
+        # Two: the kernel before it on its stream is the gather of layer i - 2,
+        # into this same view, but the wait just above (for the use of that
+        # layer) is a complete dependency and orders it first.
+        one_stream = self.sides[0] is self.sides[1]
+        flags = Z.ZERO3_GATHER_OVERLAP_PREVIOUS if i >= (1 if one_stream else 2) else 0
         Z.check(Z.zero3_gather(self.shards, self.N, self.shard, b, e, self.views[slot],
-                               self.side, flags=flags), "zero3_gather")
-        self.gathered[slot].record(self.side)
+                               side, flags=flags), "zero3_gather")
+        self.gathered[slot].record(side)
 
     def run(self, use, stream=None) -> None:
         """Calls use(i, view) for every layer in order, on ``stream``, where view
@@ -507,7 +523,8 @@ class Zero3Views:
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
         if not self.layers:
             return
-        self.side.wait_stream(s)  # the shards are ready on s
+        for side in {id(x): x for x in self.sides}.values():
+            side.wait_stream(s)  # the shards are ready on s
         self._gather(0)
         for i, (b, e) in enumerate(self.layers):
             if i + 1 < len(self.layers):
