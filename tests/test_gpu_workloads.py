@@ -58,7 +58,7 @@ def _windows(wl, psi_pad, shard, extra=(), n_random=N_RANDOM, seed=0):
     wins.append((wl.psi - WIN, psi_pad))
     for edge in (1 << 31, 1 << 32):
         if edge + WIN < psi_pad:
-            wins.append((edge - WIN // 2, edge + WIN // 2))
+            wins.append((edge - WIN, edge + WIN))     # 2^31 +- 2^20 and 2^32 +- 2^20
     splits = []
     if wl.bucket_elems:
         for k in (1, 2, 17, psi_pad // wl.bucket_elems):
@@ -112,7 +112,7 @@ def _oracle_check(oracle_mod, grads, N, scale, psi_pad):
 
 
 def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=None,
-                  device_policy=False, staging=0):
+                  device_policy=False, staging=0, pingpong=False):
     from zero_sharded_mixed_04_gb300 import synth
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     wl = synth.WORKLOADS[name]
@@ -126,7 +126,7 @@ def _run_workload(zero_lib, oracle_mod, name, out_of_place, full_compare, steps=
                    skip_on_overflow=wl.skip_on_overflow, bucket_elems=wl.bucket_elems,
                    loss_scale=wl.loss_scale, dynamic_loss_scale=wl.dynamic_loss_scale,
                    out_of_place=out_of_place, device=dev, master=master,
-                   device_policy=device_policy, smem_staging=staging)
+                   device_policy=device_policy, smem_staging=staging, pingpong=pingpong)
     del master
     _free()
     hp = oracle_mod.Hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
@@ -214,10 +214,16 @@ def test_gpt2small_n4_staged(zero_lib, oracle_mod):
 
 
 def test_flat1b_n8_as_benchmarked(zero_lib, oracle_mod):
-    """The path bench.py times: out of place, through the plan entry points,
-    with t and the loss scale kept on the device and every tile staged in
-    shared memory by TMA; the injected +inf on step 3 must be skipped and halve
-    the scale there."""
+    """The path bench.py times: out of place with ping-pong state sets, through
+    the plan entry points, with t and the loss scale kept on the device and
+    every tile staged in shared memory by TMA; the injected +inf on step 3
+    must be skipped (the current set stays current) and halve the scale."""
+    _run_workload(zero_lib, oracle_mod, "flat1b_n8", out_of_place=True, full_compare=False,
+                  device_policy=True, staging=zero_lib.ZERO_STAGING_TMA, pingpong=True)
+
+
+def test_flat1b_n8_staged_with_restore_copy(zero_lib, oracle_mod):
+    """The same without ping-pong sets: a skipped step copies src into dst."""
     _run_workload(zero_lib, oracle_mod, "flat1b_n8", out_of_place=True, full_compare=False,
                   device_policy=True, staging=zero_lib.ZERO_STAGING_TMA)
 
@@ -225,4 +231,4 @@ def test_flat1b_n8_as_benchmarked(zero_lib, oracle_mod):
 def test_flat1b_n8_register_kernel_with_device_policy(zero_lib, oracle_mod):
     """bench.py --staging registers: the same path with the register kernel."""
     _run_workload(zero_lib, oracle_mod, "flat1b_n8", out_of_place=True, full_compare=False,
-                  device_policy=True)
+                  device_policy=True, pingpong=True)
