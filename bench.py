@@ -118,8 +118,8 @@ def parse_args(argv=None):
                          "only; the benchmark line is the full size)")
     ap.add_argument("--pingpong", choices=["auto", "on", "off"], default="auto",
                     help="ping-pong state sets (the device keeps which out-of-place set is "
-                         "current, so a skipped step copies nothing); 'auto' uses them for an "
-                         "out-of-place step that can be skipped")
+                         "current, so a skipped step copies nothing and no restore kernel is "
+                         "launched); 'auto' uses them for every out-of-place step")
     seq = ap.add_mutually_exclusive_group()
     seq.add_argument("--sequence", dest="sequence", action="store_true", default=None,
                      help="also time the workload's own step sequence (fresh gradients each "
@@ -357,8 +357,7 @@ def run_ours(args, world, rank, local):
     out_of_place = not args.in_place
     device_policy = args.policy == "device" or (
         args.policy == "auto" and (wl.skip_on_overflow or wl.dynamic_loss_scale))
-    pingpong = out_of_place and (args.pingpong == "on" or (
-        args.pingpong == "auto" and wl.skip_on_overflow and not args.host_grad_accum))
+    pingpong = out_of_place and args.pingpong in ("on", "auto")
     grads = synth.make_grads(wl, 1, dev)  # step-1 gradients: no injected inf
     # the end-to-end leg's pinned host copy of the gradients, made before the
     # large device allocations as an application would hold it from the start

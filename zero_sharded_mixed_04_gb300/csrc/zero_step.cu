@@ -52,7 +52,7 @@
 namespace {
 
 constexpr int kMaxGrid = 2048;            // CTAs per launch, at most
-constexpr int kFinalizeThreads = 1024;
+constexpr int kFinalizeThreads = 256;
 constexpr int kMaxWarps = 32;             // finish_cta's per-warp slots: blocks of <= 1024 threads
 constexpr size_t kCtrlBytes = 256;
 constexpr size_t kPartialsOffset = kCtrlBytes;
@@ -776,27 +776,50 @@ __global__ void __launch_bounds__(kThreads) zero_restore_kernel(const __grid_con
 }
 
 // Step-wide decision: sums the per-CTA partials in a fixed order, forms the
-// norm and clip coefficient, decides the skip, and writes the result.
+// norm and clip coefficient, decides the skip, and writes the result.  It is
+// launched as a programmatic dependent of the step's last first-pass launch,
+// so that its launch overlaps that launch's drain; every thread first waits
+// for that grid to complete (which, through the chain of first-pass launches,
+// means every one of them has).  Without a programmatic launch the wait
+// returns at once.
 __global__ void __launch_bounds__(kFinalizeThreads)
 zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int skip_on_overflow,
                      zero_step_result* result, zero_device_policy* policy,
                      int32_t* current_set) {
-    __shared__ double s[kFinalizeThreads];
-    double t = 0.0;
-    for (int i = threadIdx.x; i < kMaxGrid; i += kFinalizeThreads) t += partials[i];
-    s[threadIdx.x] = t;
-    __syncthreads();
-    for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
-        if (threadIdx.x < w) s[threadIdx.x] += s[threadIdx.x + w];
-        __syncthreads();
-    }
+    grid_dependency_wait();
+    // each thread sums kMaxGrid / kFinalizeThreads slots in order, then a
+    // warp-shuffle tree, then the warps in order: a fixed order.  Every load
+    // is issued before the first add, so their latencies overlap.
+    constexpr int kPer = kMaxGrid / kFinalizeThreads;
+    static_assert(kMaxGrid % kFinalizeThreads == 0, "whole slots per thread");
+    double x[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) x[k] = partials[threadIdx.x + k * kFinalizeThreads];
+    // thread 0 fetches the step's flags meanwhile
+    unsigned flags_nonfinite = 0, flags_timeout = 0, flags_bounds = 0;
+    int flags_policy_error = 0;
     if (threadIdx.x == 0) {
-        const double sumsq = s[0];
+        flags_nonfinite = ctrl->nonfinite;
+        flags_timeout = ctrl->timeout;
+        flags_bounds = ctrl->bounds;
+        flags_policy_error = ctrl->policy_error;
+    }
+    double t = 0.0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) t += x[k];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    __shared__ double warp_sum[kFinalizeThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double sumsq = 0.0;
+        for (int w = 0; w < kFinalizeThreads / 32; ++w) sumsq += warp_sum[w];
         const double norm = sqrt(sumsq);
-        const int nonfinite = ctrl->nonfinite != 0u;
-        const int window_miss = (policy != nullptr && ctrl->policy_error) ? 1 : 0;
-        const int timeout = ctrl->timeout != 0u;
-        const int bounds = ctrl->bounds != 0u;   // debug build only
+        const int nonfinite = flags_nonfinite != 0u;
+        const int window_miss = (policy != nullptr && flags_policy_error) ? 1 : 0;
+        const int timeout = flags_timeout != 0u;
+        const int bounds = flags_bounds != 0u;   // debug build only
         const int skip = ((skip_on_overflow && nonfinite) || window_miss || timeout || bounds) ? 1 : 0;
         float coef = 1.0f;
         if (max_norm > 0.0 && !skip) {
@@ -1386,9 +1409,25 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
     Ctrl* ctrl = a.ctrl;
     if (result_dev == nullptr) result_dev = &ctrl->result;
 
-    zero_finalize_kernel<<<1, kFinalizeThreads, 0, stream>>>(
-        ctrl, a.partials, p->hp.max_grad_norm, p->hp.skip_on_overflow, result_dev,
-        static_cast<zero_device_policy*>(p->policy), static_cast<int32_t*>(p->current_set));
+    {
+        // a programmatic dependent of whatever kernel precedes it on the
+        // stream (normally the last bucket's last launch): it waits for that
+        // grid to complete before it reads anything
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kFinalizeThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, zero_finalize_kernel, ctrl, static_cast<const double*>(a.partials),
+                               p->hp.max_grad_norm, static_cast<int>(p->hp.skip_on_overflow),
+                               result_dev, static_cast<zero_device_policy*>(p->policy),
+                               static_cast<int32_t*>(p->current_set)) != cudaSuccess)
+            return ZERO_ERR_CUDA;
+    }
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
 
