@@ -1,7 +1,8 @@
 """Checkpoint and resume: k steps equal j steps, a save to the host, a load
 into a fresh optimizer and k - j more steps, bit for bit (state, t and the
 loss scale).  With and without the device-resident policy, in and out of
-place, with an overflowing step before the checkpoint."""
+place (out of place also with ping-pong state sets, where the device keeps
+which set is current), with an overflowing step before the checkpoint."""
 from __future__ import annotations
 
 import pytest
@@ -18,9 +19,9 @@ def _grads(N, n, step, scale):
     return out
 
 
-@pytest.mark.parametrize("out_of_place", [False, True])
+@pytest.mark.parametrize("out_of_place,pingpong", [(False, False), (True, False), (True, True)])
 @pytest.mark.parametrize("device_policy", [False, True])
-def test_resume_is_bit_exact(out_of_place, device_policy):
+def test_resume_is_bit_exact(out_of_place, pingpong, device_policy):
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
     dev = torch.device("cuda:0")
     N, n = 4, 4 * 128 * 500
@@ -29,7 +30,8 @@ def test_resume_is_bit_exact(out_of_place, device_policy):
     def make():
         return ZeroAdam(n, N, "bf16", weight_decay=0.1, skip_on_overflow=True, loss_scale=1024.0,
                         dynamic_loss_scale=True, growth_interval=2, out_of_place=out_of_place,
-                        device=dev, master=master.to(dev), device_policy=device_policy)
+                        device=dev, master=master.to(dev), device_policy=device_policy,
+                        pingpong=pingpong)
 
     def run(opt, steps):
         for s in steps:
@@ -51,3 +53,7 @@ def test_resume_is_bit_exact(out_of_place, device_policy):
     assert a.t == 4  # step 2 overflowed
     for k in ("master", "m", "v", "w"):
         assert torch.equal(a.state()[k], c.state()[k]), k
+    if pingpong:
+        # a ran 4 applied steps from set 0; c restarted from set 0 after 1
+        # applied step and applied 3 more: each ends on the set its count says
+        assert int(a.set_mem[0]) == 0 and int(c.set_mem[0]) == 1
