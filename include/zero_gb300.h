@@ -411,10 +411,15 @@ int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* policy, int
  * current BF16 working-weight view, in the set it names.  Call between
  * zero_plan_init(_ex) and zero_plan_begin.  With ZERO_STAGING_TMA both sets'
  * master/m/v must be in device memory (zero_plan_bucket returns ZERO_ERR_ARG
- * otherwise).  Returns ZERO_OK, ZERO_ERR_ARG or ZERO_ERR_OVERLAP. */
+ * otherwise).  Steps that share a word must be ordered (one stream, or
+ * events), since each reads it at its start and may write it at its end; the
+ * host must not write the word while such a step is in flight.  Returns
+ * ZERO_OK, ZERO_ERR_ARG or ZERO_ERR_OVERLAP. */
 int zero_plan_set_pingpong(zero_plan* plan, int32_t* current_set);
 
-/* Starts the step: clears the control block on `stream`. */
+/* Starts the step: clears the control block on `stream`.  With a device
+ * policy or ping-pong sets it also launches the step's one-thread prologue
+ * kernel, which reads them. */
 int zero_plan_begin(zero_plan* plan, void* stream);
 
 /* Gradient accumulation (hp->micro_batches = k >= 2; the DP-ZeRO blog,
