@@ -150,11 +150,22 @@ int zero_shard_range(const zero_layout* layout, int32_t r, int64_t* begin, int64
  * hyper-parameters.  in_place = 1 is for zero_step and 0 for zero_step_into.
  * The workspace holds:
  *   - a 256-byte control block;
- *   - per-CTA partial sums for the norm;
+ *   - per-CTA partial sums for the norm, shared by the step's launches;
  *   - when the step must see the whole gradient before it may update
  *     anything, an FP32 copy of the combined gradient (psi_pad * 4 bytes).
  *     This is needed with clipping, for an in-place step with
- *     skip_on_overflow, and (as the accumulator) with micro_batches >= 2.
+ *     skip_on_overflow, and (as the accumulator) with micro_batches >= 2;
+ *   - from the next 256-byte boundary, rows of norm partials: 256 bytes,
+ *     then 16 KiB a row.
+ *     The size returned has one row per kernel launch of the step's first
+ *     pass over the vector (a launch covers at most 2^22 elements of one
+ *     hp->bucket_elems bucket), at most 2048.
+ * A launch with a row of its own stores its CTAs' sums there; one without
+ * adds them to the shared partials after the previous launch has finished,
+ * which costs a little time.  So any size down to the part before the rows
+ * works, with the rows that fit, and every size gives a result that is the
+ * same on every run.  The norm's last bits may depend on how many rows there
+ * are.
  * Returns 0 if the arguments are invalid. */
 size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, int32_t in_place);
 
@@ -170,10 +181,11 @@ size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, int32_
  *   psi_pad, N   sizes; psi_pad must be a multiple of N * ZERO_PAD_UNIT
  *   hp           host pointer to the hyper-parameters
  *   loss_scale   > 0; the gradients hold loss_scale times the true gradient
- *   workspace    device buffer of at least zero_workspace_bytes(psi_pad, hp, 1)
- *                bytes, 256-byte aligned.  Its contents need no
- *                initialisation.  Calls that share one workspace must be
- *                ordered on one stream.
+ *   workspace    device buffer of zero_workspace_bytes(psi_pad, hp, 1) bytes
+ *                (fewer work too, down to the part before the rows of norm
+ *                partials: see zero_workspace_bytes), 256-byte aligned.  Its
+ *                contents need no initialisation.  Calls that share one
+ *                workspace must be ordered on one stream.
  *   result       device-accessible zero_step_result (device memory, or pinned
  *                host memory that the device can address), written when the
  *                step completes on `stream`; or NULL.  With NULL the call
@@ -281,6 +293,12 @@ typedef struct {
     void* current_set;                 /* ping-pong sets (zero_plan_set_pingpong): the
                                           device address of the caller's current-set
                                           word; NULL (as zero_plan_init leaves it) = off */
+    int64_t rows_offset;               /* workspace offset of the rows of norm partials */
+    int32_t row_capacity;              /* first-pass launches of a step that get a row of
+                                          their own (0: the workspace holds no rows)      */
+    int32_t rows_used;                 /* rows handed out in the current step             */
+    int32_t row_width;                 /* slots of the latest row that count               */
+    int32_t shared_slots_used;         /* 1 once a launch of the step had no row of its own */
 } zero_plan;
 
 /* Values of zero_plan.smem_staging.

@@ -147,8 +147,9 @@ def test_step_rejects_bad_workspace(zero_lib):
     assert _call(Z, ws_bytes=100) == Z.ZERO_ERR_WORKSPACE
     assert _call(Z, ws=5 * GB + 16) == Z.ZERO_ERR_WORKSPACE     # not 256-byte aligned
     hp = Z.make_hparams(skip_on_overflow=True)                   # needs the FP32 copy in place
-    small = Z.zero_workspace_bytes(4 * 128 * 4, Z.make_hparams(), True)
+    small = Z.ZERO_WORKSPACE_CONTROL_BYTES                        # enough for the one-pass step
     assert _call(Z, hp=hp, ws_bytes=small) == Z.ZERO_ERR_WORKSPACE
+    assert _call(Z, hp=hp, ws_bytes=small + 4 * 4 * 128 * 4 - 8) == Z.ZERO_ERR_WORKSPACE
 
 
 def test_step_rejects_overlap(zero_lib):
@@ -276,6 +277,25 @@ def test_accumulation_rules(zero_lib):
         assert p2.two_pass == two, kw
 
 
+@pytest.mark.parametrize("extra_rows,slack", [(0, 0), (0, 16639), (1, 0), (3, 0), (3, 16383),
+                                               (63, 0), (64, 0), (65, 0), (2048, 0), (2049, 0)])
+def test_plan_takes_the_rows_the_workspace_holds(zero_lib, extra_rows, slack):
+    """Whatever the workspace holds beyond what the step needs becomes rows of
+    norm partials: exactly as many as fit (at most 2048), none if less than
+    one fits."""
+    Z = zero_lib
+    hp = Z.make_hparams()
+    n = 4 * 128 * 4
+    base = Z.ZERO_WORKSPACE_CONTROL_BYTES
+    plan = Z.zero_plan()
+    rc = Z.zero_plan_init(plan, [6 * GB, 7 * GB, 8 * GB, 9 * GB], 0, 1 * GB, 2 * GB, 3 * GB, 4 * GB,
+                          1 * GB, 2 * GB, 3 * GB, 4 * GB, n, 4, hp, 1.0, 5 * GB,
+                          base + _rows_area(extra_rows) + slack)
+    assert rc == Z.ZERO_OK
+    assert plan.rows_offset == base
+    assert plan.row_capacity == min(extra_rows, 2048) and plan.rows_used == 0
+
+
 @pytest.mark.parametrize("layers", [[5, 9, 3, 9], [100], [], [1000, 1, 1, 999], [38_597_376, 7_082_496]])
 @pytest.mark.parametrize("N", [1, 4, 8])
 def test_zero3_peak_matches_oracle(zero_lib, oracle_mod, layers, N):
@@ -396,3 +416,44 @@ def test_layout_of_the_workload_tensor_lists(zero_lib, oracle_mod, which, N):
     for r in range(N):
         rc, b, e = zero_lib.zero_shard_range(lay, r)
         assert rc == 0 and (b, e) == (r * shard, (r + 1) * shard)
+
+
+
+def _rows_area(rows):
+    """Bytes of the rows of norm partials for `rows` launches: the carry,
+    padded to 256 bytes, then 2048 FP64 slots per row."""
+    if rows <= 0:
+        return 0
+    return 256 + rows * 2048 * 8
+
+
+def _launches(psi_pad, bucket):
+    """Launches of one pass: each bucket in near-equal parts of at most 2^22 elements."""
+    def parts(n):
+        return 0 if n <= 0 else -(-n // (1 << 22))
+    bucket = bucket or psi_pad
+    full = psi_pad // bucket
+    return min(2048, full * parts(bucket) + parts(psi_pad - full * bucket))
+
+
+@pytest.mark.parametrize("psi_pad,bucket,skip,in_place", [
+    (4 * 128 * 4, 0, False, True),                 # one launch
+    (1_000_000_512, 25_000_000, True, False),      # flat1b_n8: 40 buckets x 6 launches + 1
+    (123_589_120, 0, False, True),                 # gpt2small_n4: 30 launches
+    (6_000_000_512, 0, False, True),               # ragged6b_n4: 1431 launches
+    (3_000_000_000, 0, True, True),                # two-pass: the FP32 gradient first
+    (1 << 20, 8, False, True),                     # tiny buckets: capped at 2048 rows
+])
+def test_workspace_bytes_include_rows_of_partials(zero_lib, psi_pad, bucket, skip, in_place):
+    """zero_workspace_bytes = the part every step needs (control block and
+    shared slots, plus the FP32 combined gradient of the two-pass form), then
+    one row of norm partials per first-pass launch of the step."""
+    Z = zero_lib
+    hp = Z.make_hparams(skip_on_overflow=skip, bucket_elems=bucket)
+    need = Z.ZERO_WORKSPACE_CONTROL_BYTES + (4 * psi_pad if (skip and in_place) else 0)
+    want = -(-need // 256) * 256 + _rows_area(_launches(psi_pad, bucket))
+    assert Z.zero_workspace_bytes(psi_pad, hp, in_place) == want
+    if psi_pad == 1_000_000_512:
+        assert _launches(psi_pad, bucket) == 241
+    if psi_pad == 6_000_000_512:
+        assert _launches(psi_pad, bucket) == 1431

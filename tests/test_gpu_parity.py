@@ -665,3 +665,85 @@ def test_pingpong_skip_launches_no_copy(zero_lib):
         launches.append(Z.zero_launch_count() - before)
     assert launches[0] == launches[1] == launches[2]
     assert opt.t == 2 and int(opt.set_mem[0]) == 0
+
+
+def _rows_area(rows):
+    return 0 if rows <= 0 else 256 + rows * 2048 * 8
+
+
+@pytest.mark.parametrize("rows,bucket", [(0, 400_000), (1, 400_000), (3, 400_000), (64, 400_000),
+                                         (100, 16_384), (2048, 16_384)])
+@pytest.mark.parametrize("clip,staging", [(0.0, 0), (0.0, 1), (0.5, 0)])
+def test_norm_partials_with_few_rows(zero_lib, oracle_mod, rows, bucket, clip, staging):
+    """The workspace holds `rows` rows of norm partials for a step of many
+    first-pass launches (one per bucket): the launches beyond them add to the
+    shared slots (each waiting for the previous launch) and the first ones
+    write rows of their own.  The step, its norm and its clip must be the
+    oracle's whatever the mix.  The 16K-element buckets make 184 launches,
+    whose rows finalize sums over several CTAs."""
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, psi = 8, PSI_MULTI_SWEEP
+    psi_pad = -(-psi // (N * 128)) * (N * 128)
+    launches = -(-psi_pad // bucket)
+    grads = _make_grads(N, psi, psi_pad, "bf16", 1e-3 * 1024, 4242)
+    master = torch.zeros(psi_pad)
+    master[:psi] = torch.randn(psi, generator=torch.Generator().manual_seed(7)) * 0.02
+    src = [master.to(dev), torch.zeros(psi_pad, device=dev), torch.zeros(psi_pad, device=dev),
+           torch.zeros(psi_pad, dtype=torch.int16, device=dev)]
+    dst = [torch.empty_like(t) for t in src]
+    hp = Z.make_hparams(max_grad_norm=clip, skip_on_overflow=True, bucket_elems=bucket)
+    need = Z.ZERO_WORKSPACE_CONTROL_BYTES + (4 * psi_pad if clip > 0 else 0)
+    ws_bytes = need + _rows_area(rows)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    res = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+    plan = Z.zero_plan()
+    dev_grads = [g.to(dev) for g in grads]
+    assert Z.zero_plan_init(plan, dev_grads, Z.ZERO_GRAD_BF16, *src, *dst, psi_pad, N, hp, 1024.0,
+                            ws, ws_bytes) == Z.ZERO_OK
+    assert plan.row_capacity == rows
+    plan.smem_staging = Z.ZERO_STAGING_TMA if staging else Z.ZERO_STAGING_REGISTERS
+    assert Z.zero_plan_begin(plan, None) == Z.ZERO_OK
+    for b0 in range(0, psi_pad, bucket):
+        assert Z.zero_plan_bucket(plan, b0, min(psi_pad, b0 + bucket), None, None) == Z.ZERO_OK
+    assert plan.rows_used == min(rows, launches)
+    assert plan.shared_slots_used == (1 if rows < launches else 0)
+    assert Z.zero_plan_end(plan, res, None) == Z.ZERO_OK
+    torch.cuda.synchronize()
+    ref = _oracle_state(master.numpy())
+    ores = oracle_mod.zero_step([_np(g) for g in grads], ref["master"], ref["m"], ref["v"],
+                                ref["w"], oracle_mod.Hparams(max_grad_norm=clip), 1, 1024.0, True)
+    raw = res.clone()
+    got_res = {"applied": int(raw[0]) == Z.ZERO_OK, "found_nonfinite": bool(int(raw[1])),
+               "grad_norm": float(raw[2:3].view(torch.float32)[0]),
+               "clip_coef": float(raw[3:4].view(torch.float32)[0])}
+    compare_result(got_res, ores)
+    got = {"master": dst[0].cpu().numpy(), "m": dst[1].cpu().numpy(), "v": dst[2].cpu().numpy(),
+           "w": dst[3].cpu().numpy().view(np.uint16)}
+    compare_state(got, ref, exact=clip == 0.0)
+
+
+def test_norm_is_the_same_on_every_run(zero_lib):
+    """With rows, shared slots or a mix, the norm's sum is formed in an order
+    fixed by the sizes: the same step run again gives the same bits."""
+    Z = zero_lib
+    dev = torch.device("cuda:0")
+    N, psi_pad, bucket = 4, 2_000_896, 8192
+    g = torch.Generator(device="cpu").manual_seed(11)
+    grads = [(torch.randn(psi_pad, generator=g) * 3e-2).to(torch.bfloat16).to(dev) for _ in range(N)]
+    hp = Z.make_hparams(max_grad_norm=1.0, bucket_elems=bucket)
+    need = Z.ZERO_WORKSPACE_CONTROL_BYTES + 4 * psi_pad
+    norms = {}
+    for rows in (0, 50, 2048):
+        for rep in range(3):
+            master = torch.zeros(psi_pad, device=dev)
+            st = [master, torch.zeros_like(master), torch.zeros_like(master),
+                  torch.zeros(psi_pad, dtype=torch.int16, device=dev)]
+            ws = torch.empty(need + _rows_area(rows), dtype=torch.uint8, device=dev)
+            res = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+            assert Z.zero_step(grads, Z.ZERO_GRAD_BF16, *st, psi_pad, N, hp, 1.0, ws, ws.numel(),
+                               res) == Z.ZERO_OK
+            torch.cuda.synchronize()
+            norms.setdefault(rows, set()).add(int(res[2]))
+    for rows, bits in norms.items():
+        assert len(bits) == 1, (rows, bits)

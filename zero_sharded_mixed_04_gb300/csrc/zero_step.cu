@@ -57,6 +57,13 @@ constexpr int kMaxWarps = 32;             // finish_cta's per-warp slots: blocks
 constexpr size_t kCtrlBytes = 256;
 constexpr size_t kPartialsOffset = kCtrlBytes;
 constexpr size_t kGradOffset = kPartialsOffset + kMaxGrid * sizeof(double);  // 256-B aligned
+// Rows of norm partials (see finish_cta): one row of kMaxGrid FP64 slots per
+// first-pass launch, at most kRowCap rows, in an optional area after the part
+// of the workspace every step needs.  The area starts with the carry (the sum
+// of the rows before the latest), padded to 256 bytes, then the rows.
+constexpr int kRowCap = 2048;
+constexpr size_t kRowBytes = kMaxGrid * sizeof(double);
+constexpr size_t kRowsHeaderBytes = 256;
 
 
 // Control block at the start of the workspace.  It is zeroed at the start of
@@ -90,7 +97,13 @@ struct StepArgs {
     uint16_t* dst_w;
     const Scalars* sdev; // device policy: read the step's scalars here instead of s
     float* gws;          // FP32 combined gradient (two-pass form) or accumulator (micro-batches)
-    double* partials;    // one FP64 sum of squares per CTA
+    double* partials;    // one FP64 sum of squares per CTA: the shared slots, or this launch's row
+    const double* prev_row; // own row: the row of the step's previous launch with a row (or null)
+    double* carry;       // own row: the sum of the rows before prev_row, then with it added
+    int32_t row_width;   // own row: the slots of this row that count, at least the grid size
+    int32_t prev_width;  // own row: the same for prev_row
+    int32_t carry_in;    // own row: carry already holds the rows before prev_row
+    int32_t partial_mode;// what finish_cta does with the CTA's sum of squares (see there)
     Ctrl* ctrl;
     Scalars s;
     int64_t begin;       // first element of this launch (a multiple of kVec)
@@ -218,29 +231,85 @@ __device__ __forceinline__ void combine(const StepArgs& a, int64_t j, float (&g)
 }
 
 // End of a CTA's share: publish the overflow flag (one atomic per warp that
-// saw a non-finite value) and add the CTA's sum of squares to its FP64 slot.
-// Warp-shuffle tree, then the warps in order, so the sum is deterministic.
+// saw a non-finite value) and record the CTA's sum of squares (warp-shuffle
+// tree, then the warps in order).  Where it goes is the launch's partial mode:
+//   kOwnRow     a row of slots that belongs to this launch alone: a plain
+//               store (CTA 0 also zeroes the row's slots past the grid).
+//   kSharedSlot the one slot per CTA index that every launch without a row
+//               adds to: the add must follow the previous launch's, so thread 0
+//               of every CTA first waits for that grid to complete.  While it
+//               waits, the CTA keeps its SM slot from the next launch's CTAs.
+//   kNoPartial  nothing (the accumulate passes before the last micro-batch).
+// Launches get their own rows while the workspace has rows left; the shared
+// slots serve the rest.  In the first and last modes only CTA 0 waits for the
+// previous grid, at its very end: one waiting CTA is enough to make this grid
+// complete after the previous one, so that a pass's last launch completing
+// still means the whole pass has, and it holds one SM slot instead of all of
+// them.  With a row, CTA 0 then adds the previous launch's row, now complete,
+// to the carry: the carry gathers the rows in launch order, and finalize reads
+// only the carry and the last row.  Every sum is formed in a fixed order.
+constexpr int32_t kNoPartial = 0;
+constexpr int32_t kSharedSlot = 1;
+constexpr int32_t kOwnRow = 2;
+
+// CTA 0 of a launch with a row, every thread: wait for the previous launch,
+// then carry = (carry_in ? carry : 0) + the sum of prev_row's slots (each
+// thread its slots in order, the warp-shuffle tree, the warps in order).
+__device__ __forceinline__ void carry_previous_row(const StepArgs& a, double* warp_sum) {
+    grid_dependency_wait();
+    if (a.prev_row == nullptr) return;
+    __syncthreads();  // thread 0 has read warp_sum
+    const int width = a.prev_width < kMaxGrid ? a.prev_width : kMaxGrid;
+    double t = 0.0;
+    for (int b = static_cast<int>(threadIdx.x); b < width; b += static_cast<int>(blockDim.x))
+        t += a.prev_row[b];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double row = 0.0;
+        const int warps = static_cast<int>(blockDim.x >> 5);
+        for (int w = 0; w < warps; ++w) row += warp_sum[w];
+        *a.carry = a.carry_in ? *a.carry + row : row;
+    }
+}
+
 __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, double sumsq) {
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&a.ctrl->nonfinite, 1u);
+    if (a.partial_mode == kNoPartial) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
+        return;
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sumsq += __shfl_xor_sync(0xffffffffu, sumsq, off);
     __shared__ double warp_sum[kMaxWarps];
     if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = sumsq;
+    const bool row_cta0 = a.partial_mode == kOwnRow && blockIdx.x == 0;
+    if (row_cta0) {
+        const int width = a.row_width < kMaxGrid ? a.row_width : kMaxGrid;
+        for (int b = static_cast<int>(gridDim.x + threadIdx.x); b < width; b += blockDim.x)
+            a.partials[b] = 0.0;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         double t = 0.0;
         const int warps = static_cast<int>(blockDim.x >> 5);  // whole warps only
         for (int w = 0; w < warps; ++w) t += warp_sum[w];
-        // A bucket launch may start while the previous one drains (programmatic
-        // dependent launch).  Its slot update must still come after the
-        // previous launch's: wait for that grid to complete first.  Without a
-        // programmatic launch this returns at once.
-        grid_dependency_wait();
-        if (blockIdx.x < kMaxGrid)
-            a.partials[blockIdx.x] += t;
-        else
+        if (blockIdx.x >= kMaxGrid) {
             record_violation(a);
+        } else if (a.partial_mode == kOwnRow) {
+            a.partials[blockIdx.x] = t;
+        } else {
+            // A bucket launch may start while the previous one drains
+            // (programmatic dependent launch).  Its slot update must still
+            // come after the previous launch's: wait for that grid to complete
+            // first.  Without a programmatic launch this returns at once.
+            grid_dependency_wait();
+            a.partials[blockIdx.x] += t;
+        }
     }
+    if (row_cta0) carry_previous_row(a, warp_sum);
 }
 
 // ------------------------------------------------------------------ kernels
@@ -763,9 +832,10 @@ __global__ void __launch_bounds__(kThreads, 2) zero_update_kernel(const __grid_c
             if (range_ok(a, j[0], kVec, false)) update_groups<1>(a, s, coef, sw, j);
         }
     }
-    // A sub-launch chained to the previous one completes only after it: the
-    // step's last launch completing then means the whole pass has.
-    if (threadIdx.x == 0) grid_dependency_wait();
+    // A sub-launch chained to the previous one completes only after it (one
+    // waiting CTA is enough): the step's last launch completing then means
+    // the whole pass has.
+    if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
 }
 
 // After a one-pass out-of-place step: a skipped step must leave dst equal to
@@ -776,96 +846,103 @@ __global__ void __launch_bounds__(kThreads) zero_restore_kernel(const __grid_con
 }
 
 // Step-wide decision: sums the per-CTA partials in a fixed order, forms the
-// norm and clip coefficient, decides the skip, and writes the result.  It is
-// launched as a programmatic dependent of the step's last first-pass launch,
-// so that its launch overlaps that launch's drain; every thread first waits
-// for that grid to complete (which, through the chain of first-pass launches,
-// means every one of them has).  Without a programmatic launch the wait
-// returns at once.
-__global__ void __launch_bounds__(kFinalizeThreads)
-zero_finalize_kernel(Ctrl* ctrl, const double* partials, double max_norm, int skip_on_overflow,
-                     zero_step_result* result, zero_device_policy* policy,
-                     int32_t* current_set) {
-    grid_dependency_wait();
-    // each thread sums kMaxGrid / kFinalizeThreads slots in order, then a
-    // warp-shuffle tree, then the warps in order: a fixed order.  Every load
-    // is issued before the first add, so their latencies overlap.
-    constexpr int kPer = kMaxGrid / kFinalizeThreads;
-    static_assert(kMaxGrid % kFinalizeThreads == 0, "whole slots per thread");
-    double x[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) x[k] = partials[threadIdx.x + k * kFinalizeThreads];
-    // thread 0 fetches the step's flags meanwhile
-    unsigned flags_nonfinite = 0, flags_timeout = 0, flags_bounds = 0;
-    int flags_policy_error = 0;
-    if (threadIdx.x == 0) {
-        flags_nonfinite = ctrl->nonfinite;
-        flags_timeout = ctrl->timeout;
-        flags_bounds = ctrl->bounds;
-        flags_policy_error = ctrl->policy_error;
+// norm and clip coefficient, decides the skip, and writes the result.  One CTA,
+// launched as a programmatic dependent of the step's last first-pass launch, so
+// that its launch overlaps that launch's drain; every thread first waits for
+// that grid to complete, which (each launch completing after the one before
+// it) means every first-pass launch has.  The sum of squares is the carry (the
+// rows before the last, gathered by the launches themselves) plus the
+// block-wide sum of the shared slots (if any launch added to them) and the
+// last row: each thread its slots in order, the warp-shuffle tree, the warps
+// in order.
+__device__ __forceinline__ void decide(Ctrl* ctrl, double sumsq, double max_norm,
+                                       int skip_on_overflow, zero_step_result* result,
+                                       zero_device_policy* policy, int32_t* current_set) {
+    const double norm = sqrt(sumsq);
+    const int nonfinite = ctrl->nonfinite != 0u;
+    const int window_miss = (policy != nullptr && ctrl->policy_error) ? 1 : 0;
+    const int timeout = ctrl->timeout != 0u;
+    const int bounds = ctrl->bounds != 0u;   // debug build only
+    const int skip = ((skip_on_overflow && nonfinite) || window_miss || timeout || bounds) ? 1 : 0;
+    float coef = 1.0f;
+    if (max_norm > 0.0 && !skip) {
+        const double c = max_norm / (norm + 1e-6);
+        coef = (c < 1.0) ? static_cast<float>(c) : 1.0f;  // a NaN norm compares false
     }
+    ctrl->skip = skip;
+    ctrl->clip_coef = coef;
+    ctrl->grad_norm = static_cast<float>(norm);
+    zero_step_result r;
+    r.status = bounds        ? ZERO_ERR_BOUNDS
+               : timeout     ? ZERO_ERR_TIMEOUT
+               : window_miss ? ZERO_ERR_POLICY_WINDOW
+               : skip        ? ZERO_STEP_SKIPPED
+                             : ZERO_OK;
+    r.found_nonfinite = static_cast<uint32_t>(nonfinite);
+    r.grad_norm = static_cast<float>(norm);
+    r.clip_coef = coef;
+    *result = r;
+    // ping-pong: an applied step made the other set current.  The step's own
+    // kernels read the snapshot in ctrl->cur, never this word, so a second
+    // pass after this kernel still reads and writes the right sets.
+    if (current_set != nullptr) {
+        if (!skip) *current_set = ctrl->cur ^ 1;
+        __threadfence_system();
+    }
+    if (policy != nullptr) {
+        // the host-side rule, kept on the device: t counts applied steps; the
+        // dynamic scale backs off after an overflow, grows after
+        // growth_interval clean steps
+        if (!window_miss && !timeout && !bounds) {
+            if (!skip) policy->t += 1;
+            if (policy->growth_interval > 0) {
+                if (nonfinite) {
+                    policy->loss_scale *= policy->backoff;
+                    policy->good_steps = 0;
+                } else if (++policy->good_steps == policy->growth_interval) {
+                    policy->loss_scale *= policy->growth;
+                    policy->good_steps = 0;
+                }
+            }
+        }
+        policy->last_status = r.status;
+        __threadfence_system();
+    }
+}
+
+__global__ void __launch_bounds__(kFinalizeThreads)
+zero_finalize_kernel(Ctrl* ctrl, const double* partials, int32_t use_shared,
+                     const double* last_row, int32_t last_width, const double* carry,
+                     double max_norm, int skip_on_overflow, zero_step_result* result,
+                     zero_device_policy* policy, int32_t* current_set) {
+    grid_dependency_wait();
+    constexpr int T = kFinalizeThreads;
+    constexpr int kPer = kMaxGrid / T;
+    static_assert(kMaxGrid % T == 0, "whole slots per thread");
+    // every load issued before the first add: the shared slots, the last row
+    const int width = last_row == nullptr ? 0 : (last_width < kMaxGrid ? last_width : kMaxGrid);
+    double x[kPer], y[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int b = static_cast<int>(threadIdx.x) + k * T;
+        x[k] = use_shared ? partials[b] : 0.0;
+        y[k] = b < width ? last_row[b] : 0.0;
+    }
+    const double before = (carry != nullptr && threadIdx.x == 0) ? *carry : 0.0;
     double t = 0.0;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) t += x[k];
 #pragma unroll
+    for (int k = 0; k < kPer; ++k) t += y[k];
+#pragma unroll
     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-    __shared__ double warp_sum[kFinalizeThreads / 32];
+    __shared__ double warp_sum[T / 32];
     if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = t;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        double sumsq = 0.0;
-        for (int w = 0; w < kFinalizeThreads / 32; ++w) sumsq += warp_sum[w];
-        const double norm = sqrt(sumsq);
-        const int nonfinite = flags_nonfinite != 0u;
-        const int window_miss = (policy != nullptr && flags_policy_error) ? 1 : 0;
-        const int timeout = flags_timeout != 0u;
-        const int bounds = flags_bounds != 0u;   // debug build only
-        const int skip = ((skip_on_overflow && nonfinite) || window_miss || timeout || bounds) ? 1 : 0;
-        float coef = 1.0f;
-        if (max_norm > 0.0 && !skip) {
-            const double c = max_norm / (norm + 1e-6);
-            coef = (c < 1.0) ? static_cast<float>(c) : 1.0f;  // a NaN norm compares false
-        }
-        ctrl->skip = skip;
-        ctrl->clip_coef = coef;
-        ctrl->grad_norm = static_cast<float>(norm);
-        zero_step_result r;
-        r.status = bounds        ? ZERO_ERR_BOUNDS
-                   : timeout     ? ZERO_ERR_TIMEOUT
-                   : window_miss ? ZERO_ERR_POLICY_WINDOW
-                   : skip        ? ZERO_STEP_SKIPPED
-                                 : ZERO_OK;
-        r.found_nonfinite = static_cast<uint32_t>(nonfinite);
-        r.grad_norm = static_cast<float>(norm);
-        r.clip_coef = coef;
-        *result = r;
-        // ping-pong: an applied step made the other set current.  The step's
-        // own kernels read the snapshot in ctrl->cur, never this word, so a
-        // second pass after this kernel still reads and writes the right sets.
-        if (current_set != nullptr) {
-            if (!skip) *current_set = ctrl->cur ^ 1;
-            __threadfence_system();
-        }
-        if (policy != nullptr) {
-            // the host-side rule, kept on the device: t counts applied steps;
-            // the dynamic scale backs off after an overflow, grows after
-            // growth_interval clean steps
-            if (!window_miss && !timeout && !bounds) {
-                if (!skip) policy->t += 1;
-                if (policy->growth_interval > 0) {
-                    if (nonfinite) {
-                        policy->loss_scale *= policy->backoff;
-                        policy->good_steps = 0;
-                    } else if (++policy->good_steps == policy->growth_interval) {
-                        policy->loss_scale *= policy->growth;
-                        policy->good_steps = 0;
-                    }
-                }
-            }
-            policy->last_status = r.status;
-            __threadfence_system();
-        }
-    }
+    if (threadIdx.x != 0) return;
+    double rest = 0.0;
+    for (int w = 0; w < T / 32; ++w) rest += warp_sum[w];
+    decide(ctrl, before + rest, max_norm, skip_on_overflow, result, policy, current_set);
 }
 
 struct PolicyTable {
@@ -948,13 +1025,18 @@ struct Shape {
 
 // Persistent grid: as many CTAs as fit on the device at once (a multiple of
 // the SM count), fewer if the range is small.
-int grid_for(const void* fn, int device, int64_t n8, const Shape& sh = Shape{}) {
+// The grid of a launch with work for every resident CTA: every SM full, at
+// most kMaxGrid CTAs.
+int full_grid(const void* fn, int device, const Shape& sh = Shape{}) {
     const int64_t full =
         static_cast<int64_t>(sm_count(device)) * resident_ctas(fn, device, sh.threads, sh.smem);
+    return full > kMaxGrid ? kMaxGrid : (full < 1 ? 1 : static_cast<int>(full));
+}
+
+int grid_for(const void* fn, int device, int64_t n8, const Shape& sh = Shape{}) {
     const int64_t need = sh.tiles ? (n8 * kVec + kTile - 1) / kTile : (n8 + sh.threads - 1) / sh.threads;
-    int64_t g = need < full ? need : full;
-    if (g > kMaxGrid) g = kMaxGrid;
-    return g < 1 ? 1 : static_cast<int>(g);
+    const int full = full_grid(fn, device, sh);
+    return need < 1 ? 1 : (need < full ? static_cast<int>(need) : full);
 }
 
 // Launches fn over a.n8 groups.  With overlap_previous the launch may begin
@@ -997,9 +1079,22 @@ constexpr int64_t kLaunchAlignGroups = 32;  // 256 elements
 // sub-launches of at most kLaunchElems.  The first sub-launch overlaps the
 // kernel before it on the stream only if overlap_first; the others always
 // follow a sub-launch of the same range.
+// Where the first-pass launches of a step put their norm partials: rows of
+// their own while the workspace has rows left (see finish_cta), then the
+// shared slots.  rows == nullptr or capacity 0: the shared slots only.
+struct RowSource {
+    double* rows = nullptr;      // capacity rows of kMaxGrid slots
+    double* carry = nullptr;
+    int32_t capacity = 0;
+    int32_t* used = nullptr;     // rows handed out so far in this step
+    int32_t* width = nullptr;    // the slots of the latest row that count
+    int32_t* shared = nullptr;   // set to 1 once a launch adds to the shared slots
+    int32_t mode_without_row = kSharedSlot;
+};
+
 bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t end,
                   cudaStream_t stream, bool overlap_first, const Shape& sh = Shape{},
-                  int64_t overrun_groups = 0) {
+                  int64_t overrun_groups = 0, RowSource* rs = nullptr) {
     const int64_t groups = (end - begin) / kVec;
     if (groups <= 0) return true;
     const int64_t parts = (groups * kVec + kLaunchElems - 1) / kLaunchElems;
@@ -1014,6 +1109,25 @@ bool launch_range(StepKernel fn, int device, StepArgs a, int64_t begin, int64_t 
         a.begin = begin + g0 * kVec;
         a.n8 = (groups - g0 < per) ? groups - g0 : per;
         if (g0 + per >= groups) a.n8 += overrun_groups;  // the last launch (debug tests only)
+        if (rs != nullptr) {
+            if (rs->mode_without_row != kNoPartial && *rs->used < rs->capacity) {
+                const int32_t j = *rs->used;
+                a.partial_mode = kOwnRow;
+                a.partials = rs->rows + static_cast<int64_t>(j) * kMaxGrid;
+                // as wide as a full launch of this kernel: a shorter launch
+                // zeroes the slots past its grid
+                a.row_width = full_grid(reinterpret_cast<const void*>(fn), device, sh);
+                a.prev_row = j > 0 ? a.partials - kMaxGrid : nullptr;
+                a.prev_width = j > 0 ? *rs->width : 0;
+                a.carry = rs->carry;
+                a.carry_in = j >= 2 ? 1 : 0;
+                *rs->width = a.row_width;
+                *rs->used = j + 1;
+            } else {
+                a.partial_mode = rs->mode_without_row;
+                if (a.partial_mode == kSharedSlot) *rs->shared = 1;
+            }
+        }
         if (!launch(fn, device, a, stream, k > 0 || overlap_first, sh)) return false;
     }
     return true;
@@ -1116,11 +1230,58 @@ Scalars make_scalars(const zero_adam_hparams* hp, int32_t N, float loss_scale) {
     return s;
 }
 
+// The part of the workspace every step needs: the control block and shared
+// slots, plus the FP32 combined gradient when the step keeps one.
 size_t workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, bool in_place) {
     size_t b = kGradOffset;
     if (needs_two_passes(hp, in_place) || micro_batches_of(hp) > 1)
         b += static_cast<size_t>(psi_pad) * sizeof(float);
     return b;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Bytes of a rows area holding `rows` rows: the finalize block sums, then the
+// rows.
+size_t rows_area_bytes(int64_t rows) {
+    if (rows <= 0) return 0;
+    return kRowsHeaderBytes + static_cast<size_t>(rows) * kRowBytes;
+}
+
+// First-pass launches in one pass over psi_pad elements in buckets of
+// hp->bucket_elems (launch_range's split), at most kRowCap.
+int64_t launches_per_pass(int64_t psi_pad, const zero_adam_hparams* hp) {
+    auto parts = [](int64_t len) -> int64_t {
+        const int64_t groups = len / kVec;
+        return groups <= 0 ? 0 : (groups * kVec + kLaunchElems - 1) / kLaunchElems;
+    };
+    if (psi_pad <= 0) return 0;
+    const int64_t bucket = hp->bucket_elems > 0 ? hp->bucket_elems : psi_pad;
+    const int64_t full = psi_pad / bucket;
+    const int64_t total = (full > kRowCap ? kRowCap : full) * parts(bucket) + parts(psi_pad - full * bucket);
+    return total > kRowCap ? kRowCap : total;
+}
+
+// Rows a rows area of `avail` bytes holds.
+int32_t rows_capacity(size_t avail) {
+    if (avail <= kRowsHeaderBytes) return 0;
+    const int64_t c = static_cast<int64_t>((avail - kRowsHeaderBytes) / kRowBytes);
+    return static_cast<int32_t>(c > kRowCap ? kRowCap : c);
+}
+
+// The rows area of a plan's workspace.
+struct RowArea {
+    double* carry = nullptr;
+    double* rows = nullptr;
+};
+
+RowArea row_area(const zero_plan* p) {
+    RowArea r;
+    if (p->row_capacity <= 0) return r;
+    char* base = static_cast<char*>(p->workspace) + p->rows_offset;
+    r.carry = reinterpret_cast<double*>(base);
+    r.rows = reinterpret_cast<double*>(base + kRowsHeaderBytes);
+    return r;
 }
 
 size_t grad_elem_bytes(int32_t dtype) { return dtype == ZERO_GRAD_BF16 ? 2u : 4u; }
@@ -1138,12 +1299,14 @@ int written_spans(const zero_plan* p, Span* out) {
     add(p->dst_m, 4 * n);
     add(p->dst_v, 4 * n);
     add(p->dst_w_bf16, 2 * n);
-    if (p->grad_accum != nullptr) {
-        add(p->workspace, kGradOffset);
-        add(p->grad_accum, 4 * n);
-    } else {
-        add(p->workspace, workspace_bytes(p->psi_pad, &p->hp, p->in_place != 0));
-    }
+    // the workspace up to the end of what the step touches (its rows area too)
+    const size_t needed = p->grad_accum != nullptr ? kGradOffset
+                                                   : workspace_bytes(p->psi_pad, &p->hp, p->in_place != 0);
+    const size_t touched = p->row_capacity > 0
+                               ? static_cast<size_t>(p->rows_offset) + rows_area_bytes(p->row_capacity)
+                               : needed;
+    add(p->workspace, touched);
+    if (p->grad_accum != nullptr) add(p->grad_accum, 4 * n);
     return k;
 }
 
@@ -1188,6 +1351,7 @@ StepArgs base_args(const zero_plan* p) {
     a.limit = p->psi_pad;
     a.grad_lo = 0;
     a.grad_hi = p->psi_pad;
+    a.partial_mode = kSharedSlot;
     return a;
 }
 
@@ -1254,6 +1418,15 @@ int plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
     p.two_pass = (needs_two_passes(hp, in_place) || grad_accum != nullptr) ? 1 : 0;
     p.grad_accum = accum_dev;
     p.state = 1;
+    // whatever the workspace holds beyond what the step needs becomes rows of
+    // norm partials (see finish_cta)
+    p.rows_offset = static_cast<int64_t>(align256(need));
+    p.row_capacity = workspace_bytes_given > static_cast<size_t>(p.rows_offset)
+                         ? rows_capacity(workspace_bytes_given - static_cast<size_t>(p.rows_offset))
+                         : 0;
+    p.rows_used = 0;
+    p.row_width = 0;
+    p.shared_slots_used = 0;
 
     if (have_data) {
         const uintptr_t n = static_cast<uintptr_t>(psi_pad);
@@ -1303,6 +1476,9 @@ int plan_begin(zero_plan* p, void* stream) {
     }
     p->cursor = 0;
     p->micro_batch = 0;
+    p->rows_used = 0;
+    p->row_width = 0;
+    p->shared_slots_used = 0;
     p->state = 2;
     return ZERO_OK;
 }
@@ -1374,8 +1550,19 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     // 0.  The first bucket of a pass (begin == 0) never overlaps: when
     // accumulating it reads what the previous micro-batch wrote.
     const bool overlap = p->overlap_buckets != 0 && begin > 0;
+    // the launches' norm partials: rows of their own while the workspace has
+    // rows left; the accumulate passes before the last micro-batch have none
+    const RowArea ra = row_area(p);
+    RowSource rs;
+    rs.rows = ra.rows;
+    rs.carry = ra.carry;
+    rs.capacity = p->row_capacity;
+    rs.used = &p->rows_used;
+    rs.width = &p->row_width;
+    rs.shared = &p->shared_slots_used;
+    rs.mode_without_row = (k > 1 && p->micro_batch < k - 1) ? kNoPartial : kSharedSlot;
     if (!launch_range(fn, device, a, begin, end, static_cast<cudaStream_t>(stream), overlap, shape,
-                      end == p->psi_pad ? debug_test_overrun() : 0))
+                      end == p->psi_pad ? debug_test_overrun() : 0, &rs))
         return ZERO_ERR_CUDA;
     p->cursor = end;
     // accumulating: a micro-batch that covered the vector hands over to the
@@ -1410,9 +1597,13 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
     if (result_dev == nullptr) result_dev = &ctrl->result;
 
     {
-        // a programmatic dependent of whatever kernel precedes it on the
-        // stream (normally the last bucket's last launch): it waits for that
-        // grid to complete before it reads anything
+        // A programmatic dependent of whatever kernel precedes it on the stream
+        // (normally the last bucket's last launch); it waits for that grid to
+        // complete before it reads anything.
+        const RowArea ra = row_area(p);
+        const int32_t n_rows = p->rows_used;
+        const double* last_row = n_rows > 0 ? ra.rows + static_cast<int64_t>(n_rows - 1) * kMaxGrid
+                                            : nullptr;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1);
         cfg.blockDim = dim3(kFinalizeThreads);
@@ -1423,6 +1614,8 @@ int plan_end(zero_plan* p, zero_step_result* result, void* stream_handle) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, zero_finalize_kernel, ctrl, static_cast<const double*>(a.partials),
+                               p->shared_slots_used, last_row, n_rows > 0 ? p->row_width : 0,
+                               static_cast<const double*>(n_rows >= 2 ? ra.carry : nullptr),
                                p->hp.max_grad_norm, static_cast<int>(p->hp.skip_on_overflow),
                                result_dev, static_cast<zero_device_policy*>(p->policy),
                                static_cast<int32_t*>(p->current_set)) != cudaSuccess)
@@ -1488,7 +1681,8 @@ int run_step(const void* const* grads, int32_t grad_dtype, const float* src_mast
 extern "C" size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp,
                                        int32_t in_place) {
     if (psi_pad < 0 || hp == nullptr) return 0;
-    return workspace_bytes(psi_pad, hp, in_place != 0);
+    return align256(workspace_bytes(psi_pad, hp, in_place != 0)) +
+           rows_area_bytes(launches_per_pass(psi_pad, hp));
 }
 
 extern "C" int zero_step(const void* const* grads, int32_t grad_dtype, float* master, float* m,

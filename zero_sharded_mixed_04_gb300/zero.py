@@ -91,7 +91,10 @@ class zero_plan(ctypes.Structure):
                 ("state", ctypes.c_int32), ("micro_batch", ctypes.c_int32),
                 ("policy_t_count", ctypes.c_int32), ("policy_t_first", ctypes.c_int64),
                 ("policy", ctypes.c_void_p), ("overlap_buckets", ctypes.c_int32),
-                ("smem_staging", ctypes.c_int32), ("current_set", ctypes.c_void_p)]
+                ("smem_staging", ctypes.c_int32), ("current_set", ctypes.c_void_p),
+                ("rows_offset", ctypes.c_int64), ("row_capacity", ctypes.c_int32),
+                ("rows_used", ctypes.c_int32), ("row_width", ctypes.c_int32),
+                ("shared_slots_used", ctypes.c_int32)]
 
 
 class zero_device_policy(ctypes.Structure):
