@@ -5,6 +5,9 @@ runs them; this file is not collected by pytest itself.
   parity   a few steps of every kernel form (one-pass register and staged,
            two-pass, accumulation, ping-pong sets, the ZeRO-3 gather) against
            the oracle, bit for bit; the kernels' checks must find nothing.
+  sweep    the first 128 configurations of the random parity sweep
+           (test_gpu_sweep.py), each against the oracle; the checks must find
+           nothing in any of them.
   overrun  with ZERO_DEBUG_TEST_OVERRUN set, the last launch of each pass
            covers groups past the end of the buffers.  Every buffer is
            allocated with a guard region behind it that is larger than the
@@ -202,5 +205,18 @@ def overrun() -> None:
     print("debug build overrun: ok")
 
 
+def sweep() -> None:
+    import oracle
+    from test_gpu_sweep import draw_case, run_case
+    from zero_sharded_mixed_04_gb300 import zero as Z
+    assert Z.DEBUG_BUILD and Z.LIB_PATH.endswith("libzero_gb300_debug.so")
+    oracle.build()
+    for seed in range(128):
+        run_case(draw_case(seed), oracle)
+    n = Z.zero_debug_bounds_violations()
+    assert n == 0, f"the debug build's checks skipped {n} accesses in the sweep"
+    print("debug build sweep: ok")
+
+
 if __name__ == "__main__":
-    {"parity": parity, "overrun": overrun}[sys.argv[1]]()
+    {"parity": parity, "overrun": overrun, "sweep": sweep}[sys.argv[1]]()

@@ -4,6 +4,7 @@ lengths of the buffers before touching it; nothing traps.
 
 * parity: correct runs of every kernel form match the oracle and the checks
   find nothing;
+* sweep: the same for 128 configurations of the random parity sweep;
 * overrun: launches made to run past the end of the buffers (a debug-only
   test setting) have every out-of-range access skipped and counted, end with
   ZERO_ERR_BOUNDS, and leave the guard regions behind every buffer as they
@@ -36,6 +37,10 @@ def _run(case, extra_env=None):
 
 def test_debug_build_parity(zero_lib):
     assert "debug build parity: ok" in _run("parity")
+
+
+def test_debug_build_random_sweep(zero_lib):
+    assert "debug build sweep: ok" in _run("sweep")
 
 
 def test_debug_build_skips_out_of_range_accesses(zero_lib):

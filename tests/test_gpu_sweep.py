@@ -88,10 +88,10 @@ def _np(t):
     return t.numpy()
 
 
-@pytest.mark.parametrize("seed", range(N_CASES))
-def test_random_configuration(zero_lib, oracle_mod, seed):
+def run_case(case: dict, oracle_mod) -> None:
+    """The case's three steps through ZeroAdam, each checked against the oracle."""
     from zero_sharded_mixed_04_gb300.optim import ZeroAdam
-    case = draw_case(seed)
+    seed = case["seed"]
     dev = torch.device("cuda:0")
     psi, psi_pad = case["psi"], case["psi_pad"]
     master = torch.zeros(psi_pad)
@@ -137,6 +137,11 @@ def test_random_configuration(zero_lib, oracle_mod, seed):
                                                            ores["found_nonfinite"], 2, 0.5, 2.0)
         assert opt.t == o_t and opt.scaler.scale == o_scale, tag
         compare_state(state_to_numpy(opt.state()), ref, exact, tag=tag)
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_configuration(zero_lib, oracle_mod, seed):
+    run_case(draw_case(seed), oracle_mod)
 
 
 def test_sweep_covers_the_options():
