@@ -120,6 +120,10 @@ def parse_args(argv=None):
                     help="ping-pong state sets (the device keeps which out-of-place set is "
                          "current, so a skipped step copies nothing and no restore kernel is "
                          "launched); 'auto' uses them for every out-of-place step")
+    ap.add_argument("--profile-step", type=int, default=-1,
+                    help="bracket timed step K (0-based) with cudaProfilerStart/Stop, so that "
+                         "ncu --profile-from-start off --replay-mode app-range measures that "
+                         "step's launches as one range, overlapping as they run")
     seq = ap.add_mutually_exclusive_group()
     seq.add_argument("--sequence", dest="sequence", action="store_true", default=None,
                      help="also time the workload's own step sequence (fresh gradients each "
@@ -423,7 +427,11 @@ def run_ours(args, world, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
+        if k == args.profile_step:
+            torch.cuda.profiler.start()
         one_step(k)
+        if k == args.profile_step:
+            torch.cuda.profiler.stop()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     if not opt.last_result(stream)["applied"]:
