@@ -122,7 +122,7 @@ def parse_args(argv=None):
                          "launched); 'auto' uses them for every out-of-place step")
     ap.add_argument("--profile-step", type=int, default=-1,
                     help="bracket timed step K (0-based) with cudaProfilerStart/Stop, so that "
-                         "ncu --profile-from-start off --replay-mode app-range measures that "
+                         "ncu --replay-mode app-range measures that "
                          "step's launches as one range, overlapping as they run")
     seq = ap.add_mutually_exclusive_group()
     seq.add_argument("--sequence", dest="sequence", action="store_true", default=None,
