@@ -120,6 +120,12 @@ def parse_args(argv=None):
                     help="ping-pong state sets (the device keeps which out-of-place set is "
                          "current, so a skipped step copies nothing and no restore kernel is "
                          "launched); 'auto' uses them for every out-of-place step")
+    ap.add_argument("--profile-graph", action="store_true",
+                    help="before the timed steps, capture one step as a CUDA graph and replay "
+                         "it between cudaProfilerStart/Stop, so that an ncu range capture holds "
+                         "one graph launch instead of the step's host calls (needs the device "
+                         "policy and ping-pong sets, which keep the step's host state on the "
+                         "device)")
     ap.add_argument("--profile-step", type=int, default=-1,
                     help="bracket timed step K (0-based) with cudaProfilerStart/Stop, so that "
                          "ncu --replay-mode app-range measures that "
@@ -411,6 +417,33 @@ def run_ours(args, world, rank, local):
     for k in range(args.warmup):
         one_step(k)
     torch.cuda.synchronize(dev)
+    if args.profile_graph:
+        # One more step, captured as a graph and replayed once inside the
+        # profiler range (once only: the captured prologue holds a window of one
+        # t).  Capturing runs nothing and changes no host state here: with the
+        # device policy and ping-pong sets, t, the loss scale and the current
+        # set all live on the device.
+        if not (device_policy and pingpong and k_micro == 1):
+            raise SystemExit("--profile-graph needs the device policy and ping-pong sets")
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap, capture_error_mode="relaxed"):
+            opt.enqueue(grads, cap, api=args.api)
+        torch.cuda.synchronize(dev)
+        # every step noted as in flight has completed, and the one noted while
+        # capturing was never recorded on a running stream: forget them all
+        opt._inflight.clear()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.profiler.start()
+        g0.record(stream)
+        graph.replay()
+        g1.record(stream)
+        torch.cuda.profiler.stop()
+        torch.cuda.synchronize(dev)
+        if not opt.last_result(stream)["applied"]:
+            raise RuntimeError("the profiled graph step was skipped")
+        print(f"graph step: {g0.elapsed_time(g1):.4f} ms", file=sys.stderr)
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)

@@ -1522,8 +1522,14 @@ int plan_bucket(zero_plan* p, int64_t begin, int64_t end, const void* const* buc
     if (k == 1 && !p->two_pass && p->smem_staging != ZERO_STAGING_REGISTERS) {
         fn = pick<StagedK>(p->N, bf16);
         if (!staged_shape(fn, device, p->N, bf16, a, shape)) return ZERO_ERR_ARG;
-        for (int i = 0; i < p->N; ++i)
-            if (!device_memory(a.grads[i])) return ZERO_ERR_ARG;
+        // the plan's own gradient buffers once per pass (at its first bucket),
+        // a bucket's own pointers every time
+        if (bucket_grads != nullptr || begin == 0)
+            for (int i = 0; i < p->N; ++i)
+                if (!device_memory(a.grads[i])) return ZERO_ERR_ARG;
+        if (begin == 0 && bucket_grads != nullptr)
+            for (int i = 0; i < p->N; ++i)
+                if (p->grads[i] != nullptr && !device_memory(p->grads[i])) return ZERO_ERR_ARG;
         if (begin == 0 &&
             (!device_memory(p->src_master) || !device_memory(p->src_m) || !device_memory(p->src_v)))
             return ZERO_ERR_ARG;
