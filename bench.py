@@ -64,7 +64,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 # the step kernels' code: the profile summaries are tied to a hash of these
 KERNEL_SOURCES = [os.path.join(ROOT, "zero_sharded_mixed_04_gb300", "csrc", f)
-                  for f in ("zero_step.cu", "zero_elem.cuh", "zero_common.cuh")]
+                  for f in ("zero_kernels.cuh", "zero_elem.cuh", "zero_common.cuh")]
 # the committed ncu summary of each one-pass kernel on the full flat1b_n8 workload
 PROFILE_SUMMARY = {
     "zero_fused_kernel": os.path.join(ROOT, "profiles", "zero_fused_kernel_flat1b_n8.md"),

@@ -24,7 +24,7 @@ DEBUG_LIB_PATH = os.path.join(PKG, "libzero_gb300_debug.so")
 
 SOURCES = ["zero_step.cu", "zero3_gather.cu", "zero_host.cpp"]
 HEADERS = [os.path.join(INCLUDE, "zero_gb300.h"), os.path.join(CSRC, "zero_common.cuh"),
-           os.path.join(CSRC, "zero_elem.cuh")]
+           os.path.join(CSRC, "zero_elem.cuh"), os.path.join(CSRC, "zero_kernels.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               f"-I{INCLUDE}"]
