@@ -50,3 +50,21 @@ def test_bench_line_keeps_the_contract(zero_lib):
     assert seq["steps"] == 10 and len(seq["ms"]) == 10 and seq["skipped_steps"] == []
     c = d["clocks"]
     assert "sm_mhz" in c and "reasons" in c
+
+
+def test_profile_graph_replays_one_real_step(zero_lib):
+    """--profile-graph captures one step as a CUDA graph and replays it between
+    cudaProfilerStart/Stop (the range ncu measures as a unit); the replayed step
+    applies, and the timed steps after it still run and keep the line's shape."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "gpt2small_n4",
+                        "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-e2e",
+                        "--no-sequence", "--policy", "device", "--profile-graph"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert "graph step:" in r.stderr
+    ms = float(r.stderr.split("graph step:")[1].split("ms")[0])
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    d = json.loads(lines[-1])
+    # the replayed step does the work of an eager one, within launch overheads
+    assert 0.5 * d["ms_per_step"] < ms < 3.0 * d["ms_per_step"], (ms, d["ms_per_step"])
+    assert d["config"]["step_policy"] == "device"
