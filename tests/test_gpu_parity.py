@@ -747,3 +747,19 @@ def test_norm_is_the_same_on_every_run(zero_lib):
             norms.setdefault(rows, set()).add(int(res[2]))
     for rows, bits in norms.items():
         assert len(bits) == 1, (rows, bits)
+
+
+@pytest.mark.parametrize("sigma,dtype,clip", [
+    (1e25, "fp32", 1.0),    # squares overflow FP32: the norm stays finite and the clip bites
+    (1e25, "fp32", 0.0),    # the norm is reported; Adam's own g*g overflows on both sides
+    (3e30, "bf16", 1.0),
+    (1e-30, "fp32", 0.0),   # squares underflow FP32: the norm is still reported
+    (1e-30, "fp32", 1e-28),
+    (1e-40, "fp32", 0.0),   # subnormal gradients: the divisions' and roots' slow paths
+])
+def test_norm_of_extreme_magnitudes(zero_lib, oracle_mod, sigma, dtype, clip):
+    """The global norm is the square root of the exact sum of squares (the
+    oracle sums FP64 squares).  Gradients whose FP32 squares would overflow or
+    underflow must give the oracle's norm and clip coefficient all the same."""
+    run_parity(zero_lib, oracle_mod, N=4, psi=PSI_SMALL, dtype=dtype, steps=2, clip=clip,
+               sigma=sigma, loss_scale=1.0)

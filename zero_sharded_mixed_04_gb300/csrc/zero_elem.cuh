@@ -35,6 +35,33 @@ __device__ __forceinline__ bool is_nonfinite(float x) {
     return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
 }
 
+// Sum of squares of K values, in FP64, without the overflow (|x| >= 2^64) or
+// underflow (|x| < 2^-75) that squaring in FP32 meets.  The values are
+// multiplied by one power of two, 2^-e, where 2^e is the binade of their
+// largest magnitude (clamped so that 2^-e stays a normal FP32 number).  The
+// scaled squares are summed in FP32 in order, by multiply-add, and the sum is
+// multiplied by 2^(2e) in FP64, exactly.  Multiplying by a power of two
+// commutes with rounding in the normal range, so wherever the unscaled squares
+// neither overflow nor underflow this gives the bits of summing them unscaled.
+// A NaN or an infinity reaches the result through its own square.
+template <int K>
+__device__ __forceinline__ double sum_of_squares(const float (&x)[K]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < K; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+    e = e < -126 ? -126 : (e > 126 ? 126 : e);
+    const float s = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    float sq = 0.0f;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        const float y = __fmul_rn(x[i], s);
+        sq = fmaf(y, y, sq);
+    }
+    return static_cast<double>(sq) *
+           __longlong_as_double(static_cast<long long>(1023 + 2 * e) << 52);
+}
+
 // BF16 is the top half of an FP32 word; element 2q of a 16-byte vector is the
 // low half of 32-bit word q.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -340,16 +340,15 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s
     for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
             float gs = __fmul_rn(g[u][e], s.inv);
             if constexpr (kAccIn) gs = __fadd_rn(acc[u][e], gs);
             bad |= is_nonfinite(gs) ? 1u : 0u;
-            sq = fmaf(gs, gs, sq);
+            g[u][e] = gs;
             adam_element(gs, p[u][e], m[u][e], v[u][e], s);
         }
-        sumsq += static_cast<double>(sq);
+        sumsq += sum_of_squares(g[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -544,15 +543,14 @@ __device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s
     const float4 M = lds_f4(state + (kTile + e) * 4);
     const float4 V = lds_f4(state + (2 * kTile + e) * 4);
     float p[4] = {P.x, P.y, P.z, P.w}, m[4] = {M.x, M.y, M.z, M.w}, v[4] = {V.x, V.y, V.z, V.w};
-    float sq = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float gs = __fmul_rn(g[q], s.inv);
         bad |= is_nonfinite(gs) ? 1u : 0u;
-        sq = fmaf(gs, gs, sq);
+        g[q] = gs;
         adam_element(gs, p[q], m[q], v[q], s);
     }
-    sumsq += static_cast<double>(sq);
+    sumsq += sum_of_squares(g);
     __stcs(reinterpret_cast<float4*>(out_master(a, sw) + j), make_float4(p[0], p[1], p[2], p[3]));
     __stcs(reinterpret_cast<float4*>(out_m(a, sw) + j), make_float4(m[0], m[1], m[2], m[3]));
     __stcs(reinterpret_cast<float4*>(out_v(a, sw) + j), make_float4(v[0], v[1], v[2], v[3]));
@@ -666,14 +664,12 @@ __device__ __forceinline__ void reduce_groups(const StepArgs& a, const Scalars& 
     for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
             g[u][e] = __fmul_rn(g[u][e], s.inv);
             bad |= is_nonfinite(g[u][e]) ? 1u : 0u;
-            sq = fmaf(g[u][e], g[u][e], sq);
         }
-        sumsq += static_cast<double>(sq);
+        sumsq += sum_of_squares(g[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) store8(a.gws, j[u], g[u]);
@@ -723,14 +719,12 @@ __device__ __forceinline__ void accum_groups(const StepArgs& a, const Scalars& s
     for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
             acc[u][e] = __fadd_rn(acc[u][e], __fmul_rn(g[u][e], s.inv));
             bad |= is_nonfinite(acc[u][e]) ? 1u : 0u;
-            sq = fmaf(acc[u][e], acc[u][e], sq);
         }
-        if (a.acc_last) sumsq += static_cast<double>(sq);
+        if (a.acc_last) sumsq += sum_of_squares(acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) store8(a.gws, j[u], acc[u]);
