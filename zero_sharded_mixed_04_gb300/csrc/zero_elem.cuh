@@ -45,7 +45,7 @@ __device__ __forceinline__ bool is_nonfinite(float x) {
 // neither overflow nor underflow this gives the bits of summing them unscaled.
 // A NaN or an infinity reaches the result through its own square.
 template <int K>
-__device__ __forceinline__ double sum_of_squares(const float (&x)[K]) {
+__device__ __forceinline__ double sum_of_squares_scaled(const float (&x)[K]) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < K; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -60,6 +60,24 @@ __device__ __forceinline__ double sum_of_squares(const float (&x)[K]) {
     }
     return static_cast<double>(sq) *
            __longlong_as_double(static_cast<long long>(1023 + 2 * e) << 52);
+}
+
+// The same sum, unscaled where that is exact.  A finite FP32 sum means no
+// partial sum overflowed.  A sum of at least 2^-40 means that any square which
+// underflowed lay far below half a unit in the last place of the sum (the
+// multiply-add rounds only once, after the exact product), so scaling would
+// not change a bit.  Other groups, rare, take the scaled sum.
+__device__ __forceinline__ bool squares_in_range(float sq) {
+    return sq >= 0x1p-40f && sq < INFINITY;
+}
+
+template <int K>
+__device__ __forceinline__ double sum_of_squares(const float (&x)[K]) {
+    float sq = 0.0f;
+#pragma unroll
+    for (int i = 0; i < K; ++i) sq = fmaf(x[i], x[i], sq);
+    if (squares_in_range(sq)) return static_cast<double>(sq);
+    return sum_of_squares_scaled(x);
 }
 
 // BF16 is the top half of an FP32 word; element 2q of a 16-byte vector is the

@@ -317,6 +317,20 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 
 // ------------------------------------------------------------------ kernels
 
+// One 8-element group's combined gradient, formed as fused_groups forms it.
+template <int NT, bool kBF16, bool kAccIn>
+__device__ __forceinline__ void combined_gradient(const StepArgs& a, const Scalars& s, int64_t j,
+                                                  float (&g)[kVec]) {
+    float acc[kVec];
+    if constexpr (kAccIn) load8(a.gws, j, acc);
+    combine<NT, kBF16>(a, j, g);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+        g[e] = __fmul_rn(g[e], s.inv);
+        if constexpr (kAccIn) g[e] = __fadd_rn(acc[e], g[e]);
+    }
+}
+
 // One 8-element group: reduce-scatter + scale + check + Adam + BF16 all-gather.
 // kAccIn: the last micro-batch of an accumulated step.  The combined gradient
 // is this micro-batch's scaled contribution added to the FP32 accumulator the
@@ -325,7 +339,7 @@ __device__ __forceinline__ void finish_cta(const StepArgs& a, unsigned bad, doub
 template <int NT, bool kBF16, bool kAccIn, int U>
 __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s, bool sw,
                                              const int64_t (&j)[U], unsigned& bad,
-                                             double& sumsq) {
+                                             double& sumsq, unsigned& extreme) {
     float p[U][kVec], m[U][kVec], v[U][kVec], g[U][kVec];
     float acc[kAccIn ? U : 1][kVec];
     // every load of the U groups is issued before any arithmetic
@@ -340,15 +354,18 @@ __device__ __forceinline__ void fused_groups(const StepArgs& a, const Scalars& s
     for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+        float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
             float gs = __fmul_rn(g[u][e], s.inv);
             if constexpr (kAccIn) gs = __fadd_rn(acc[u][e], gs);
             bad |= is_nonfinite(gs) ? 1u : 0u;
-            g[u][e] = gs;
+            sq = fmaf(gs, gs, sq);
             adam_element(gs, p[u][e], m[u][e], v[u][e], s);
         }
-        sumsq += sum_of_squares(g[u]);
+        // out of range: the kernel sums this thread's groups again, scaled
+        extreme |= squares_in_range(sq) ? 0u : 1u;
+        sumsq += static_cast<double>(sq);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -376,19 +393,46 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
     // FP32 gradients plus the accumulator do not fit two groups in 128
     // registers without spilling: those take one group at a time.
     constexpr bool kPairs = kBF16 || !kAccIn;
+    unsigned extreme = 0;
+    const int64_t q0 = q;
     for (; kPairs && q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
         if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
-        fused_groups<NT, kBF16, kAccIn, 2>(a, s, sw, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 2>(a, s, sw, j, bad, sumsq, extreme);
     }
     for (; !kPairs && q + stride < n8; q += stride) {
         const int64_t j[1] = {a.begin + q * kVec};
         if (!range_ok(a, j[0], kVec, true)) continue;
-        fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
+        fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq, extreme);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        if (range_ok(a, j[0], kVec, true)) fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq);
+        if (range_ok(a, j[0], kVec, true))
+            fused_groups<NT, kBF16, kAccIn, 1>(a, s, sw, j, bad, sumsq, extreme);
+    }
+    if (extreme) {
+        // The same groups in the same order, their combined gradient formed
+        // again from the inputs (which this kernel only reads), summed scaled.
+        sumsq = 0.0;
+        float g[kVec];
+        for (q = q0; kPairs && q + stride < n8; q += 2 * stride) {
+            const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+            if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                combined_gradient<NT, kBF16, kAccIn>(a, s, j[u], g);
+                sumsq += sum_of_squares(g);
+            }
+        }
+        for (; !kPairs && q + stride < n8; q += stride) {
+            if (!range_ok(a, a.begin + q * kVec, kVec, true)) continue;
+            combined_gradient<NT, kBF16, kAccIn>(a, s, a.begin + q * kVec, g);
+            sumsq += sum_of_squares(g);
+        }
+        if (q < n8 && range_ok(a, a.begin + q * kVec, kVec, true)) {
+            combined_gradient<NT, kBF16, kAccIn>(a, s, a.begin + q * kVec, g);
+            sumsq += sum_of_squares(g);
+        }
     }
     finish_cta(a, bad, sumsq);
 }
@@ -654,22 +698,28 @@ __global__ void __launch_bounds__(kStagedThreads)
     finish_cta(a, bad, sumsq);
 }
 
-// U groups of the first pass of the two-pass form.
+// U groups of the first pass of the two-pass form.  The squares are summed
+// unscaled; a group whose FP32 sum is out of range sets `extreme`, and the
+// kernel then sums this thread's groups again, scaled (sum_of_squares), from
+// the combined gradient it wrote.  That keeps the common loop free of a branch.
 template <int NT, bool kBF16, int U>
 __device__ __forceinline__ void reduce_groups(const StepArgs& a, const Scalars& s,
                                               const int64_t (&j)[U], unsigned& bad,
-                                              double& sumsq) {
+                                              double& sumsq, unsigned& extreme) {
     float g[U][kVec];
 #pragma unroll
     for (int u = 0; u < U; ++u) combine<NT, kBF16>(a, j[u], g[u]);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+        float sq = 0.0f;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
             g[u][e] = __fmul_rn(g[u][e], s.inv);
             bad |= is_nonfinite(g[u][e]) ? 1u : 0u;
+            sq = fmaf(g[u][e], g[u][e], sq);
         }
-        sumsq += sum_of_squares(g[u]);
+        extreme |= squares_in_range(sq) ? 0u : 1u;
+        sumsq += static_cast<double>(sq);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) store8(a.gws, j[u], g[u]);
@@ -687,14 +737,34 @@ __global__ void __launch_bounds__(kThreads, 2) zero_reduce_kernel(const __grid_c
     const int64_t n8 = policy_off(a) ? 0 : a.n8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     int64_t q = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    unsigned extreme = 0;
+    const int64_t q0 = q;
     for (; q + stride < n8; q += 2 * stride) {
         const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
         if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
-        reduce_groups<NT, kBF16, 2>(a, s, j, bad, sumsq);
+        reduce_groups<NT, kBF16, 2>(a, s, j, bad, sumsq, extreme);
     }
     if (q < n8) {
         const int64_t j[1] = {a.begin + q * kVec};
-        if (range_ok(a, j[0], kVec, true)) reduce_groups<NT, kBF16, 1>(a, s, j, bad, sumsq);
+        if (range_ok(a, j[0], kVec, true)) reduce_groups<NT, kBF16, 1>(a, s, j, bad, sumsq, extreme);
+    }
+    if (extreme) {
+        // the same groups in the same order, from the values this thread stored
+        sumsq = 0.0;
+        float g[kVec];
+        for (q = q0; q + stride < n8; q += 2 * stride) {
+            const int64_t j[2] = {a.begin + q * kVec, a.begin + (q + stride) * kVec};
+            if (!range_ok(a, j[0], kVec, true) || !range_ok(a, j[1], kVec, true)) continue;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                load8(a.gws, j[u], g);
+                sumsq += sum_of_squares(g);
+            }
+        }
+        if (q < n8 && range_ok(a, a.begin + q * kVec, kVec, true)) {
+            load8(a.gws, a.begin + q * kVec, g);
+            sumsq += sum_of_squares(g);
+        }
     }
     finish_cta(a, bad, sumsq);
 }
