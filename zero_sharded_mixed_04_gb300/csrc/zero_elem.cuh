@@ -62,11 +62,12 @@ __device__ __forceinline__ double sum_of_squares_scaled(const float (&x)[K]) {
            __longlong_as_double(static_cast<long long>(1023 + 2 * e) << 52);
 }
 
-// The same sum, unscaled where that is exact.  A finite FP32 sum means no
-// partial sum overflowed.  A sum of at least 2^-40 means that any square which
-// underflowed lay far below half a unit in the last place of the sum (the
-// multiply-add rounds only once, after the exact product), so scaling would
-// not change a bit.  Other groups, rare, take the scaled sum.
+// The same sum, unscaled where that gives the same bits.  A finite FP32 sum
+// means no partial sum overflowed.  The multiply-add forms each square
+// exactly, so the only coarse rounding a small value can meet is that of a
+// partial sum in the subnormal range, off by at most 2^-150.  Against a final
+// sum of at least 2^-40, whose half unit in the last place is 2^-65 or more,
+// that cannot change a bit.  Other groups, rare, take the scaled sum.
 __device__ __forceinline__ bool squares_in_range(float sq) {
     return sq >= 0x1p-40f && sq < INFINITY;
 }
