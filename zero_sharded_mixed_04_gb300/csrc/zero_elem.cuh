@@ -62,12 +62,14 @@ __device__ __forceinline__ double sum_of_squares_scaled(const float (&x)[K]) {
            __longlong_as_double(static_cast<long long>(1023 + 2 * e) << 52);
 }
 
-// The same sum, unscaled where that gives the same bits.  A finite FP32 sum
-// means no partial sum overflowed.  The multiply-add forms each square
-// exactly, so the only coarse rounding a small value can meet is that of a
-// partial sum in the subnormal range, off by at most 2^-150.  Against a final
-// sum of at least 2^-40, whose half unit in the last place is 2^-65 or more,
-// that cannot change a bit.  Other groups, rare, take the scaled sum.
+// The same sum, unscaled where that is as accurate.  A finite FP32 sum means
+// no partial sum overflowed.  The multiply-add forms each square exactly, so
+// the only coarse rounding a small value can meet is that of a partial sum in
+// the subnormal range, off by at most 2^-150.  Against a final sum of at least
+// 2^-40, whose half unit in the last place is 2^-65 or more, that gives the
+// scaled sum's bits unless the exact sum lies within 2^-150 of a rounding
+// boundary, and one unit in the last place at worst.  Other groups, rare, take
+// the scaled sum.  Either way the result is a fixed function of the values.
 __device__ __forceinline__ bool squares_in_range(float sq) {
     return sq >= 0x1p-40f && sq < INFINITY;
 }
