@@ -439,10 +439,10 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
 
 // ------------------------------------------------------------------ staged one-pass kernel
 //
-// The same one-pass step with each tile of kTile elements staged in shared
+// The same one-pass step with each tile of T::kTile elements staged in shared
 // memory.  One producer thread copies a tile's N gradient chunks and its
 // master/m/v chunks from HBM into a stage with TMA bulk copies
-// (cp.async.bulk), counted in the stage's "full" mbarrier.  Sixteen consumer
+// (cp.async.bulk), counted in the stage's "full" mbarrier.  The consumer
 // warps wait on it, compute from shared memory, store the results straight to
 // HBM and arrive on the stage's "empty" mbarrier, which the producer waits on
 // before it refills the stage.  Two stages per CTA: one tile is computed from
@@ -468,12 +468,25 @@ __global__ void __launch_bounds__(kThreads, 2) zero_fused_kernel(const __grid_co
 // global store of a warp is one contiguous run.  The element arithmetic is
 // the register kernel's.
 
-constexpr int kTile = 2048;
-constexpr int kStagedConsumerWarps = 16;
-constexpr int kStagedConsumers = 32 * kStagedConsumerWarps;
-constexpr int kStagedThreads = kStagedConsumers + 32;  // + the producer warp
-static_assert(kTile % (4 * kStagedConsumers) == 0, "whole 4-element chunks per consumer");
-static_assert(kStagedThreads <= 32 * kMaxWarps, "finish_cta's per-warp slots");
+// The tile, per kernel instance: 2048 elements and 16 consumer warps, or 1536
+// and 12 where an element's bytes (N*g + 12) are at most 25, so that three
+// CTAs of two stages fit one SM's shared memory instead of two.  Measured
+// interleaved on one GPU: GPT-2 small, N = 4 BF16, 0.621 ms per step against
+// 0.637 with 2048; ragged 6B, N = 4, 29.12 ms against 29.52; Psi = 1e9, N = 8
+// (57 KB stages either way two CTAs) 6.020 against 6.018; 1280 and 10 warps
+// (three CTAs for N = 8) 6.034.  A runtime rank count (NT = 0) keeps 2048.
+constexpr int staged_tile(int nt, bool bf16) {
+    return (nt > 0 && nt * (bf16 ? 2 : 4) + 12 <= 25) ? 1536 : 2048;
+}
+template <int NT, bool kBF16>
+struct Staged {
+    static constexpr int kTile = staged_tile(NT, kBF16);
+    static constexpr int kWarps = kTile / 128;        // consumer warps: 4 elements a thread
+    static constexpr int kConsumers = 32 * kWarps;
+    static constexpr int kThreads = kConsumers + 32;  // + the producer warp
+    static_assert(kTile % (4 * kConsumers) == 0, "whole 4-element chunks per consumer");
+    static_assert(kThreads <= 32 * kMaxWarps, "finish_cta's per-warp slots");
+};
 constexpr int kMaxStages = 2;
 constexpr size_t kStagedSmemLimit = 200 * 1024;  // dynamic shared memory per CTA, at most
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
@@ -567,7 +580,7 @@ __device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s
     // rank order from +0, as in the register kernel
 #pragma unroll(NT > 0 ? NT : 1)
     for (int i = 0; i < n; ++i) {
-        const unsigned char* chunk = st + static_cast<size_t>(i) * kTile * gbytes;
+        const unsigned char* chunk = st + static_cast<size_t>(i) * Staged<NT, kBF16>::kTile * gbytes;
         if constexpr (kBF16) {
             const uint2 r = lds_u2(chunk + e * 2);
             g[0] = __fadd_rn(g[0], bf16_lo(r.x));
@@ -582,6 +595,7 @@ __device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s
             g[3] = __fadd_rn(g[3], r.w);
         }
     }
+    constexpr int kTile = Staged<NT, kBF16>::kTile;
     const unsigned char* state = st + static_cast<size_t>(n) * kTile * gbytes;
     const float4 P = lds_f4(state + e * 4);
     const float4 M = lds_f4(state + (kTile + e) * 4);
@@ -603,9 +617,12 @@ __device__ __forceinline__ void staged_chunk(const StepArgs& a, const Scalars& s
 }
 
 template <int NT, bool kBF16>
-__global__ void __launch_bounds__(kStagedThreads)
+__global__ void __launch_bounds__(Staged<NT, kBF16>::kThreads)
     zero_fused_staged_kernel(const __grid_constant__ StepArgs a) {
     allow_next_launch();
+    constexpr int kTile = Staged<NT, kBF16>::kTile;
+    constexpr int kStagedConsumerWarps = Staged<NT, kBF16>::kWarps;
+    constexpr int kStagedConsumers = Staged<NT, kBF16>::kConsumers;
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr uint32_t gbytes = kBF16 ? 2 : 4;
     const int n_ranks = NT > 0 ? NT : a.N;

@@ -49,9 +49,13 @@ struct AccumK {
     static constexpr StepKernel fn = zero_accum_kernel<NT, B>;
 };
 
+// The rank count a kernel instance is compiled for: N itself for 1, 2, 4 and
+// 8, else 0 (the instance that reads N at run time).
+int compiled_ranks(int N) { return (N == 1 || N == 2 || N == 4 || N == 8) ? N : 0; }
+
 template <template <int, bool> class K>
 StepKernel pick(int N, bool bf16) {
-    switch (N) {
+    switch (compiled_ranks(N)) {
         case 1: return bf16 ? K<1, true>::fn : K<1, false>::fn;
         case 2: return bf16 ? K<2, true>::fn : K<2, false>::fn;
         case 4: return bf16 ? K<4, true>::fn : K<4, false>::fn;
@@ -62,12 +66,12 @@ StepKernel pick(int N, bool bf16) {
 
 
 // Launch shape of a step kernel: the register kernels take one 8-element group
-// per thread and no dynamic shared memory; the staged kernel one kTile tile
-// per CTA and `smem` bytes of stages.
+// per thread and no dynamic shared memory; the staged kernel one tile of
+// `tile` elements per CTA and `smem` bytes of stages.
 struct Shape {
     int threads = kThreads;
     size_t smem = 0;
-    bool tiles = false;
+    int tile = 0;  // 0: not tiled
 };
 
 // Persistent grid: as many CTAs as fit on the device at once (a multiple of
@@ -81,7 +85,8 @@ int full_grid(const void* fn, int device, const Shape& sh = Shape{}) {
 }
 
 int grid_for(const void* fn, int device, int64_t n8, const Shape& sh = Shape{}) {
-    const int64_t need = sh.tiles ? (n8 * kVec + kTile - 1) / kTile : (n8 + sh.threads - 1) / sh.threads;
+    const int64_t need = sh.tile > 0 ? (n8 * kVec + sh.tile - 1) / sh.tile
+                                     : (n8 + sh.threads - 1) / sh.threads;
     const int full = full_grid(fn, device, sh);
     return need < 1 ? 1 : (need < full ? static_cast<int>(need) : full);
 }
@@ -196,7 +201,8 @@ bool device_memory(const void* ptr) {
 // kMaxStages) in kStagedSmemLimit, at least two.  Fills a.stages,
 // a.stage_bytes and the launch shape; false if two stages do not fit.
 bool staged_shape(StepKernel fn, int device, int N, bool bf16, StepArgs& a, Shape& sh) {
-    const size_t stage = static_cast<size_t>(N) * kTile * (bf16 ? 2 : 4) + 3 * size_t(kTile) * 4;
+    const int tile = staged_tile(compiled_ranks(N), bf16);  // the instance pick<StagedK> chose
+    const size_t stage = static_cast<size_t>(N) * tile * (bf16 ? 2 : 4) + 3 * size_t(tile) * 4;
     int stages = kMaxStages;
     while (stages >= 2 && stages * (stage + 16) > kStagedSmemLimit) --stages;
     if (stages < 2) return false;
@@ -215,9 +221,9 @@ bool staged_shape(StepKernel fn, int device, int N, bool bf16, StepArgs& a, Shap
     }
     a.stages = stages;
     a.stage_bytes = static_cast<uint32_t>(stage);
-    sh.threads = kStagedThreads;
+    sh.threads = 32 * (tile / 128) + 32;  // Staged<NT, bf16>::kThreads
     sh.smem = stages * stage + 2 * stages * sizeof(uint64_t);
-    sh.tiles = true;
+    sh.tile = tile;
     return true;
 }
 
