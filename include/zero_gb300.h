@@ -304,15 +304,17 @@ typedef struct {
 /* Values of zero_plan.smem_staging.
  *   ZERO_STAGING_REGISTERS  every thread loads its 8-element groups from HBM
  *                           straight into registers, two groups in flight.
- *   ZERO_STAGING_TMA        one thread per CTA copies each 2048-element tile
+ *   ZERO_STAGING_TMA        one thread per CTA copies each tile of T elements
  *                           (the N gradient chunks and the master/m/v chunks)
  *                           into one of two shared-memory stages with TMA bulk
- *                           copies; sixteen warps compute from shared memory.
+ *                           copies; T / 128 warps compute from shared memory.
+ *                           T is 2048, or 1536 for N = 1, 2 or 4 with
+ *                           N * g <= 13, where three CTAs then fit an SM.
  *                           Alternating the chunks between two slots, one
  *                           computed from while the other fills, is the DP-ZeRO
- *                           blog's two-buffer pattern.  Needs 2 * (N * 2048 * g + 24576) bytes of
- *                           shared memory per CTA, at most 200 KB (g = 2 for
- *                           BF16 gradients, 4 for FP32: N <= 18 and N <= 9),
+ *                           blog's two-buffer pattern.  Needs 2 * T * (N * g + 12)
+ *                           bytes of shared memory per CTA, at most 200 KB (g = 2
+ *                           for BF16 gradients, 4 for FP32: N <= 18 and N <= 9),
  *                           and the gradients and src master/m/v in device
  *                           memory (the copies read no pinned host or managed
  *                           memory); otherwise zero_plan_bucket returns
