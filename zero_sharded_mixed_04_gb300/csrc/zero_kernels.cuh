@@ -28,7 +28,7 @@
 //     registers, two 8-element groups in flight, every load of a group issued
 //     before its arithmetic;
 //   - zero_fused_staged_kernel: one thread per CTA copies each tile into
-//     shared memory with TMA bulk copies, and sixteen warps compute from there.
+//     shared memory with TMA bulk copies, and 12 or 16 warps compute from there.
 // The arithmetic uses the explicit round-to-nearest intrinsics, so no
 // multiply-add is ever contracted: each element is rounded operator by
 // operator.
