@@ -77,6 +77,9 @@ MUTANTS = {
         "        acc[j] = 0.0f;\n    for (int32_t mb = 0; mb < k; ++mb)",
         "        acc[j] = orc_reduce_element(grads, dtype, N, j, inv);\n"
         "    for (int32_t mb = 1; mb < k; ++mb)"),
+    "norm_squares_in_fp32": (
+        "s = s + (double)g[j] * (double)g[j];",
+        "s = s + (double)(g[j] * g[j]);"),
     "accumulation_mean_without_k": (
         "float inv = (float)(1.0 / ((double)N * (double)k * loss_scale));",
         "float inv = (float)(1.0 / ((double)N * loss_scale));"),

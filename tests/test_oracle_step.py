@@ -136,3 +136,26 @@ def test_windowed_form_equals_whole_step(oracle_mod, clip):
             a[win] = p
     for a, b in zip((master, m, v, w), whole):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+@pytest.mark.parametrize("c", [1e30, 1e25, 3e19, 1.0, 1e-20, 1e-30, 1e-40])
+def test_norm_is_the_closed_form_at_any_magnitude(oracle_mod, c):
+    """Every rank sends the same FP32 gradient c, so the batch-mean gradient is
+    c in every one of the n elements, to within the rounding of the FP32 rank
+    sum (N = 4, loss scale 1), and its norm is |c| * sqrt(n).  That holds where c*c overflows FP32 (c >= 2^64)
+    or underflows it (c < 2^-75): the norm is the square root of the sum of
+    squares, not of a sum that saturated."""
+    N, n = 4, 4 * 128 * 8
+    g = np.full(n, c, np.float32)
+    cf = float(np.float32(c))            # the value FP32 holds (1e-40 is subnormal)
+    master = np.zeros(n, np.float32)
+    m, v, w = np.zeros_like(master), np.zeros_like(master), np.zeros(n, np.uint16)
+    res = oracle_mod.zero_step([g] * N, master, m, v, w, oracle_mod.Hparams(), 1, 1.0)
+    want = abs(cf) * math.sqrt(n)
+    assert res["grad_norm"] == pytest.approx(want, rel=1e-6)
+    # with a clip bound the coefficient follows from that norm
+    master = np.zeros(n, np.float32)
+    m, v, w = np.zeros_like(master), np.zeros_like(master), np.zeros(n, np.uint16)
+    res = oracle_mod.zero_step([g] * N, master, m, v, w, oracle_mod.Hparams(max_grad_norm=1.0), 1,
+                               1.0)
+    assert res["clip_coef"] == pytest.approx(min(1.0, 1.0 / (want + 1e-6)), rel=1e-6)
