@@ -64,6 +64,10 @@ extern "C" {
 #define ZERO_MAX_RANKS 64      /* largest N accepted                           */
 #define ZERO_ALIGN_BYTES 16    /* every buffer must start on this boundary     */
 #define ZERO_BUCKET_ALIGN 8    /* bucket_elems must be a multiple of this      */
+/* Largest element count any entry point accepts (psi, psi_pad, a shard, a
+ * layer): 2^48, 1 PiB of FP32, past any device's memory.  Larger counts are
+ * refused as bad arguments, so no byte size formed from one can overflow. */
+#define ZERO_MAX_ELEMS (1LL << 48)
 
 typedef enum {
     ZERO_OK = 0,              /* success; for a step: the update was applied       */
@@ -138,7 +142,8 @@ typedef struct {
  *   out             host struct, filled on success
  *   tensor_offsets  host array of n_tensors int64 (caller-owned) that receives
  *                   each tensor's start in the flat vector; may be NULL
- * Returns ZERO_OK or ZERO_ERR_ARG (nothing written on error).  Host only. */
+ * Returns ZERO_OK or ZERO_ERR_ARG (nothing written on error; also when the
+ * padded total would exceed ZERO_MAX_ELEMS).  Host only. */
 int zero_init_layout(const int64_t* tensor_numel, int64_t n_tensors, int32_t N,
                      zero_layout* out, int64_t* tensor_offsets);
 
@@ -178,7 +183,8 @@ size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp, int32_
  *                Owner r's slice is [r*S, (r+1)*S).
  *   w_bf16       device array of psi_pad BF16 values (uint16 bit patterns):
  *                the full working-weight view that the all-gather fills
- *   psi_pad, N   sizes; psi_pad must be a multiple of N * ZERO_PAD_UNIT
+ *   psi_pad, N   sizes; psi_pad must be a multiple of N * ZERO_PAD_UNIT and at
+ *                most ZERO_MAX_ELEMS
  *   hp           host pointer to the hyper-parameters
  *   loss_scale   > 0; the gradients hold loss_scale times the true gradient
  *   workspace    device buffer of zero_workspace_bytes(psi_pad, hp, 1) bytes
@@ -507,8 +513,9 @@ int zero_plan_end(zero_plan* plan, zero_step_result* result, void* stream);
  * is read from shards[j / shard] at offset j % shard.
  *   shards   host array of N device pointers, each ZERO_ALIGN_BYTES-aligned,
  *            holding `shard` BF16 values
- *   shard    elements per shard, a multiple of ZERO_BUCKET_ALIGN (every
- *            layout from zero_init_layout qualifies)
+ *   shard    elements per shard, a multiple of ZERO_BUCKET_ALIGN, with N * shard
+ *            at most ZERO_MAX_ELEMS (every layout from zero_init_layout
+ *            qualifies)
  *   view     device buffer of end - begin BF16 values, ZERO_ALIGN_BYTES-aligned;
  *            it must not overlap a shard
  *   flags    0 or ZERO3_GATHER_OVERLAP_PREVIOUS
@@ -541,7 +548,8 @@ int64_t zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers, int32_t N
  * 16/N bytes per parameter.  See the DP-ZeRO blog's stage table, and RC-T2
  * note N47: 128/56/44/32 GB for 8e9 parameters on 4 ranks.  GB there means
  * 1e9 bytes, counting persistent state only.  Host only.
- * Returns -1 on a bad argument. */
+ * Returns -1 on a bad argument (psi outside 0 .. ZERO_MAX_ELEMS, N < 1, a byte
+ * width outside 0 .. 64). */
 int64_t zero_ledger(int64_t psi, int32_t N, int32_t stage, int32_t grad_bytes,
                     int32_t optim_bytes);
 

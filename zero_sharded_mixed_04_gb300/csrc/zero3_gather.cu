@@ -121,7 +121,8 @@ extern "C" int zero3_gather(const uint16_t* const* shards, int32_t N, int64_t sh
                             int64_t end, uint16_t* view, uint32_t flags, void* stream) {
     NvtxRange range("zero3_gather");
     if (shards == nullptr || N < 1 || N > ZERO_MAX_RANKS || shard < 0 || shard % kVec != 0 ||
-        begin < 0 || end < begin || end > static_cast<int64_t>(N) * shard ||
+        shard > ZERO_MAX_ELEMS / N || begin < 0 || end < begin ||
+        end > static_cast<int64_t>(N) * shard ||
         (flags & ~ZERO3_GATHER_OVERLAP_PREVIOUS) != 0)
         return ZERO_ERR_ARG;
     const int64_t n = end - begin;

@@ -28,9 +28,10 @@ extern "C" int zero_init_layout(const int64_t* tensor_numel, int64_t n_tensors, 
         return ZERO_ERR_ARG;
     int64_t psi = 0;
     for (int64_t i = 0; i < n_tensors; ++i) {
-        if (tensor_numel[i] < 0 || psi > INT64_MAX / 2 - tensor_numel[i]) return ZERO_ERR_ARG;
+        if (tensor_numel[i] < 0 || tensor_numel[i] > ZERO_MAX_ELEMS - psi) return ZERO_ERR_ARG;
         psi += tensor_numel[i];
     }
+    if (psi > ZERO_MAX_ELEMS - static_cast<int64_t>(N) * ZERO_PAD_UNIT) return ZERO_ERR_ARG;
     // second pass writes the offsets only once every size is known to be valid
     if (tensor_offsets != nullptr) {
         int64_t at = 0;
@@ -60,7 +61,9 @@ extern "C" int zero_shard_range(const zero_layout* layout, int32_t r, int64_t* b
 
 extern "C" int64_t zero_ledger(int64_t psi, int32_t N, int32_t stage, int32_t grad_bytes,
                                int32_t optim_bytes) {
-    if (psi < 0 || N < 1 || grad_bytes < 0 || optim_bytes < 0) return -1;
+    if (psi < 0 || psi > ZERO_MAX_ELEMS || N < 1 || grad_bytes < 0 || grad_bytes > 64 ||
+        optim_bytes < 0 || optim_bytes > 64)
+        return -1;
     const int64_t weight = 2;  // BF16 working weight
     const int64_t grad = grad_bytes;
     const int64_t optim = optim_bytes;
@@ -80,7 +83,7 @@ extern "C" int64_t zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers
     int64_t psi = 0;
     int64_t live = 0;  // the most elements alive in the two views at once
     for (int64_t i = 0; i < n_layers; ++i) {
-        if (layer_numel[i] < 0) return -1;
+        if (layer_numel[i] < 0 || layer_numel[i] > ZERO_MAX_ELEMS - psi) return -1;
         psi += layer_numel[i];
         const int64_t next = (i + 1 < n_layers) ? layer_numel[i + 1] : 0;
         if (layer_numel[i] + next > live) live = layer_numel[i] + next;
@@ -91,7 +94,7 @@ extern "C" int64_t zero3_peak_bytes(const int64_t* layer_numel, int64_t n_layers
 }
 
 extern "C" int64_t zero_comm_volume(int64_t psi, int32_t N, int32_t stage) {
-    if (psi < 0 || N < 1 || stage < 0 || stage > 3) return -1;
+    if (psi < 0 || psi > ZERO_MAX_ELEMS || N < 1 || stage < 0 || stage > 3) return -1;
     // reduce-scatter + all-gather (= one all-reduce); ZeRO-3 gathers the
     // weights once more
     return (stage == 3 ? 3 : 2) * psi;

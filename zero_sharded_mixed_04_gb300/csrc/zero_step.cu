@@ -416,7 +416,7 @@ int plan_init(zero_plan* plan, const void* const* grads, int32_t grad_dtype,
               bool allow_null_grads, float* grad_accum = nullptr) {
     if (plan == nullptr) return ZERO_ERR_ARG;
     const bool in_place = (dst_master == src_master);
-    if (grads == nullptr || N < 1 || N > ZERO_MAX_RANKS || psi_pad < 0 ||
+    if (grads == nullptr || N < 1 || N > ZERO_MAX_RANKS || psi_pad < 0 || psi_pad > ZERO_MAX_ELEMS ||
         (grad_dtype != ZERO_GRAD_BF16 && grad_dtype != ZERO_GRAD_FP32) || !valid_hparams(hp) ||
         !(loss_scale > 0.0f) || !std::isfinite(loss_scale))
         return ZERO_ERR_ARG;
@@ -739,7 +739,7 @@ int run_step(const void* const* grads, int32_t grad_dtype, const float* src_mast
 
 extern "C" size_t zero_workspace_bytes(int64_t psi_pad, const zero_adam_hparams* hp,
                                        int32_t in_place) {
-    if (psi_pad < 0 || hp == nullptr) return 0;
+    if (psi_pad < 0 || psi_pad > ZERO_MAX_ELEMS || hp == nullptr) return 0;
     return align256(workspace_bytes(psi_pad, hp, in_place != 0)) +
            rows_area_bytes(launches_per_pass(psi_pad, hp));
 }

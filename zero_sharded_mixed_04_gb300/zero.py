@@ -31,6 +31,7 @@ ZERO_PAD_UNIT = 128
 ZERO_MAX_RANKS = 64
 ZERO_ALIGN_BYTES = 16
 ZERO_BUCKET_ALIGN = 8
+ZERO_MAX_ELEMS = 1 << 48
 
 ZERO_OK = 0
 ZERO_STEP_SKIPPED = 1
