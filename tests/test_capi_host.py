@@ -192,6 +192,30 @@ def test_loss_scaler_matches_oracle_policy(oracle_mod):
     assert static.scale == 8.0
 
 
+def test_constants_match_the_header(zero_lib, tmp_path):
+    """Every integer #define and enum value of include/zero_gb300.h has the
+    binding's value (checked against a program gcc compiles from the header)."""
+    import re
+    import subprocess
+    header = open(os.path.join(ROOT, "include", "zero_gb300.h")).read()
+    names = [n for n in re.findall(r"^#define (ZERO\w+) \S", header, re.M)]
+    names += re.findall(r"^\s+(ZERO_(?:OK|STEP_\w+|ERR_\w+|GRAD_\w+))\s*=", header, re.M)
+    assert {"ZERO_MAX_ELEMS", "ZERO_OK", "ZERO_ERR_BOUNDS", "ZERO_GRAD_FP32",
+            "ZERO_NOALLOC_SCRATCH_BYTES"} <= set(names)
+    src = tmp_path / "consts.c"
+    src.write_text("\n".join(["#include <stdio.h>", '#include "zero_gb300.h"', "int main(void) {"] +
+                             [f'printf("{n} %lld\\n", (long long)({n}));' for n in names] +
+                             ["return 0; }"]))
+    exe = tmp_path / "consts"
+    subprocess.run(["gcc", "-std=c11", f"-I{os.path.join(ROOT, 'include')}", str(src), "-o",
+                    str(exe)], check=True)
+    out = dict(line.split() for line in subprocess.run(
+        [str(exe)], check=True, capture_output=True, text=True).stdout.splitlines())
+    for n in names:
+        assert hasattr(zero_lib, n), f"the binding has no {n}"
+        assert int(out[n]) == getattr(zero_lib, n), n
+
+
 def test_struct_layouts_match_the_header(zero_lib, tmp_path):
     """The ctypes mirrors of the header's structs have the C sizes and offsets
     (checked against a program gcc compiles from include/zero_gb300.h)."""
