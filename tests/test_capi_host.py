@@ -372,6 +372,7 @@ def test_pingpong_argument_checks(zero_lib):
     """zero_plan_set_pingpong wants an initialised out-of-place plan whose two
     sets are complete and disjoint.  Fake addresses: every call here is
     rejected before any CUDA call."""
+    torch = pytest.importorskip("torch")
     Z = zero_lib
     N, n = 4, 4 * 128 * 4
     grads = [6 * GB + i * GB // 4 for i in range(N)]
@@ -481,3 +482,59 @@ def test_workspace_bytes_include_rows_of_partials(zero_lib, psi_pad, bucket, ski
         assert _launches(psi_pad, bucket) == 241
     if psi_pad == 6_000_000_512:
         assert _launches(psi_pad, bucket) == 1431
+
+
+def test_binding_pads_a_short_gradient_list(zero_lib):
+    """Fewer gradient pointers than N reach the library as NULLs, an argument
+    error, never as a read past the end of the pointer array."""
+    Z = zero_lib
+    hp = Z.make_hparams()
+    n = 4 * 128 * 4
+    ws = Z.zero_workspace_bytes(n, hp, True)
+    rc = Z.zero_step([6 * GB, 7 * GB, 8 * GB], Z.ZERO_GRAD_BF16, 1 * GB, 2 * GB, 3 * GB, 4 * GB,
+                     n, 4, hp, 1.0, 5 * GB, ws, None, 0)
+    assert rc == Z.ZERO_ERR_ARG
+    # a plan may take its gradients per bucket: the missing ranks stay NULL
+    plan = Z.zero_plan()
+    assert Z.zero_plan_init(plan, [6 * GB], Z.ZERO_GRAD_BF16, 1 * GB, 2 * GB, 3 * GB, 4 * GB,
+                            1 * GB, 2 * GB, 3 * GB, 4 * GB, n, 4, hp, 1.0, 5 * GB, ws) == 0
+    assert plan.grads[0] == 6 * GB and not any(plan.grads[1:4])
+    assert Z.zero3_gather([6 * GB], 4, 1024, 0, 8, 5 * GB, 0, 0) == Z.ZERO_ERR_ARG
+
+
+def test_binding_refuses_tensors_too_small_for_the_call(zero_lib):
+    """Torch tensors passed as buffers must hold what the call touches and be
+    contiguous; the binding refuses them before the library sees a pointer."""
+    torch = pytest.importorskip("torch")
+    Z = zero_lib
+    N, n = 4, 4 * 128 * 4
+    hp = Z.make_hparams()
+    ws = torch.empty(Z.zero_workspace_bytes(n, hp, True), dtype=torch.uint8)
+    grads = [torch.zeros(n, dtype=torch.bfloat16) for _ in range(N)]
+    st = [torch.zeros(n), torch.zeros(n), torch.zeros(n), torch.zeros(n, dtype=torch.int16)]
+
+    def call(g=grads, s=st, w=ws, wsb=ws.numel(), dtype=Z.ZERO_GRAD_BF16):
+        return Z.zero_step(g, dtype, *s, n, N, hp, 1.0, w, wsb, None, 0)
+
+    with pytest.raises(ValueError, match=r"grads\[2\]"):
+        call(g=grads[:2] + [torch.zeros(n - 8, dtype=torch.bfloat16)] + grads[3:])
+    with pytest.raises(ValueError, match=r"grads\[0\]"):   # FP32 gradients need 4 bytes each
+        call(dtype=Z.ZERO_GRAD_FP32)
+    with pytest.raises(ValueError, match="w_bf16"):
+        call(s=st[:3] + [torch.zeros(n // 2, dtype=torch.int16)])
+    with pytest.raises(ValueError, match="not contiguous"):
+        call(s=[torch.zeros(2 * n)[::2]] + st[1:])
+    with pytest.raises(ValueError, match="workspace"):
+        call(wsb=ws.numel() + 1)
+    with pytest.raises(ValueError, match="view"):
+        Z.zero3_gather([torch.zeros(1024, dtype=torch.int16)] * N, N, 1024, 0, 2048,
+                       torch.zeros(1024, dtype=torch.int16), 0, 0)
+    plan = Z.zero_plan()
+    plan.grad_dtype, plan.N, plan.psi_pad = Z.ZERO_GRAD_BF16, N, n
+    with pytest.raises(ValueError, match=r"bucket_grads\[1\]"):
+        Z.zero_plan_bucket(plan, 0, 512, [torch.zeros(512, dtype=torch.bfloat16),
+                                          torch.zeros(256, dtype=torch.bfloat16)], 0)
+    # a size the library refuses is left for it to refuse, whatever the buffers hold
+    small = torch.zeros(8, dtype=torch.int16)
+    assert Z.zero3_gather([small] * N, N, 1024, 0, 4097, small, 0, 0) == Z.ZERO_ERR_ARG
+    assert Z.zero_plan_bucket(plan, 0, n + 512, [small] * N, 0) == Z.ZERO_ERR_ARG

@@ -221,14 +221,55 @@ def zero_workspace_bytes(psi_pad: int, hp: zero_adam_hparams, in_place: bool) ->
     return _lib.zero_workspace_bytes(psi_pad, ctypes.byref(hp), int(bool(in_place)))
 
 
-def _grad_array(grads):
-    return (ctypes.c_void_p * max(len(grads), 1))(*[_addr(g) for g in grads])
+def _grad_array(grads, N=None):
+    """The C array of gradient pointers, padded with NULLs to N entries: a list
+    shorter than N reaches the library as missing gradients (an argument error),
+    never as a read past the end of the array."""
+    n = len(grads)
+    if N is not None:
+        n = max(n, min(max(int(N), 0), ZERO_MAX_RANKS))
+    ptrs = [_addr(g) for g in grads] + [None] * (n - len(grads))
+    return (ctypes.c_void_p * max(n, 1))(*ptrs)
+
+
+def _check(x, nbytes: int, name: str) -> None:
+    """A torch tensor handed over as a buffer must be contiguous and hold the
+    nbytes the call will touch.  Raw addresses are the caller's to size."""
+    if x is None or not hasattr(x, "data_ptr") or nbytes <= 0:
+        return
+    if not x.is_contiguous():
+        raise ValueError(f"{name}: the tensor is not contiguous")
+    have = x.numel() * x.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name}: the tensor holds {have} bytes, the call uses {nbytes}")
+
+
+def _check_step(grads, grad_dtype: int, psi_pad: int, state, workspace=None,
+                workspace_bytes: int = 0) -> None:
+    """The sizes a step reads and writes: N gradients of psi_pad elements,
+    FP32 master/m/v and BF16 weights of psi_pad elements, the workspace."""
+    if not 0 < psi_pad <= ZERO_MAX_ELEMS:
+        return  # sizes the library refuses are left for it to refuse
+    g = 2 if grad_dtype == ZERO_GRAD_BF16 else 4
+    for i, t in enumerate(grads):
+        _check(t, psi_pad * g, f"grads[{i}]")
+    for name, t, elem in state:
+        _check(t, psi_pad * elem, name)
+    _check(workspace, workspace_bytes, "workspace")
+
+
+def _state(prefix, master, m, v, w):
+    return [(prefix + "master", master, 4), (prefix + "m", m, 4), (prefix + "v", v, 4),
+            (prefix + "w_bf16", w, 2)]
 
 
 def zero_step(grads, grad_dtype: int, master, m, v, w_bf16, psi_pad: int, N: int,
               hp: zero_adam_hparams, loss_scale: float, workspace, workspace_bytes: int,
               result=None, stream=None) -> int:
-    return _lib.zero_step(_grad_array(grads), grad_dtype, _addr(master), _addr(m), _addr(v),
+    _check_step(grads, grad_dtype, psi_pad, _state("", master, m, v, w_bf16), workspace,
+                workspace_bytes)
+    _check(result, 16, "result")
+    return _lib.zero_step(_grad_array(grads, N), grad_dtype, _addr(master), _addr(m), _addr(v),
                           _addr(w_bf16), psi_pad, N, ctypes.byref(hp), loss_scale,
                           _addr(workspace), workspace_bytes, _addr(result), _stream(stream))
 
@@ -237,7 +278,11 @@ def zero_step_into(grads, grad_dtype: int, src_master, src_m, src_v, src_w_bf16,
                    dst_m, dst_v, dst_w_bf16, psi_pad: int, N: int, hp: zero_adam_hparams,
                    loss_scale: float, workspace, workspace_bytes: int, result=None,
                    stream=None) -> int:
-    return _lib.zero_step_into(_grad_array(grads), grad_dtype, _addr(src_master), _addr(src_m),
+    _check_step(grads, grad_dtype, psi_pad,
+                _state("src_", src_master, src_m, src_v, src_w_bf16) +
+                _state("dst_", dst_master, dst_m, dst_v, dst_w_bf16), workspace, workspace_bytes)
+    _check(result, 16, "result")
+    return _lib.zero_step_into(_grad_array(grads, N), grad_dtype, _addr(src_master), _addr(src_m),
                                _addr(src_v), _addr(src_w_bf16), _addr(dst_master), _addr(dst_m),
                                _addr(dst_v), _addr(dst_w_bf16), psi_pad, N, ctypes.byref(hp),
                                loss_scale, _addr(workspace), workspace_bytes, _addr(result),
@@ -248,7 +293,10 @@ def zero_plan_init(plan: zero_plan, grads, grad_dtype: int, src_master, src_m, s
                    dst_master, dst_m, dst_v, dst_w_bf16, psi_pad: int, N: int,
                    hp: zero_adam_hparams, loss_scale: float, workspace,
                    workspace_bytes: int) -> int:
-    return _lib.zero_plan_init(ctypes.byref(plan), _grad_array(grads), grad_dtype,
+    _check_step(grads, grad_dtype, psi_pad,
+                _state("src_", src_master, src_m, src_v, src_w_bf16) +
+                _state("dst_", dst_master, dst_m, dst_v, dst_w_bf16), workspace, workspace_bytes)
+    return _lib.zero_plan_init(ctypes.byref(plan), _grad_array(grads, N), grad_dtype,
                                _addr(src_master), _addr(src_m), _addr(src_v), _addr(src_w_bf16),
                                _addr(dst_master), _addr(dst_m), _addr(dst_v), _addr(dst_w_bf16),
                                psi_pad, N, ctypes.byref(hp), loss_scale, _addr(workspace),
@@ -259,7 +307,11 @@ def zero_plan_init_ex(plan: zero_plan, grads, grad_dtype: int, src_master, src_m
                       src_w_bf16, dst_master, dst_m, dst_v, dst_w_bf16, psi_pad: int, N: int,
                       hp: zero_adam_hparams, loss_scale: float, workspace, workspace_bytes: int,
                       grad_accum=None) -> int:
-    return _lib.zero_plan_init_ex(ctypes.byref(plan), _grad_array(grads), grad_dtype,
+    _check_step(grads, grad_dtype, psi_pad,
+                _state("src_", src_master, src_m, src_v, src_w_bf16) +
+                _state("dst_", dst_master, dst_m, dst_v, dst_w_bf16) +
+                [("grad_accum", grad_accum, 4)], workspace, workspace_bytes)
+    return _lib.zero_plan_init_ex(ctypes.byref(plan), _grad_array(grads, N), grad_dtype,
                                   _addr(src_master), _addr(src_m), _addr(src_v),
                                   _addr(src_w_bf16), _addr(dst_master), _addr(dst_m),
                                   _addr(dst_v), _addr(dst_w_bf16), psi_pad, N, ctypes.byref(hp),
@@ -285,11 +337,18 @@ def zero_plan_begin(plan: zero_plan, stream=None) -> int:
 
 def zero_plan_bucket(plan: zero_plan, begin: int, end: int, bucket_grads=None,
                      stream=None) -> int:
-    arr = None if bucket_grads is None else _grad_array(bucket_grads)
+    arr = None
+    if bucket_grads is not None:
+        g = 2 if plan.grad_dtype == ZERO_GRAD_BF16 else 4
+        if 0 <= begin < end <= plan.psi_pad:
+            for i, t in enumerate(bucket_grads):
+                _check(t, (end - begin) * g, f"bucket_grads[{i}]")
+        arr = _grad_array(bucket_grads, plan.N)
     return _lib.zero_plan_bucket(ctypes.byref(plan), begin, end, arr, _stream(stream))
 
 
 def zero_plan_end(plan: zero_plan, result=None, stream=None) -> int:
+    _check(result, 16, "result")
     return _lib.zero_plan_end(ctypes.byref(plan), _addr(result), _stream(stream))
 
 
@@ -298,7 +357,9 @@ def zero_step_noalloc(grads, grad_dtype: int, master, m, v, w_bf16, psi_pad: int
                       stream=None) -> int:
     """zero_step with the library's fixed scratch array as its workspace, for
     callers that cannot allocate device memory (see include/zero_gb300.h)."""
-    return _lib.zero_step_noalloc(_grad_array(grads), grad_dtype, _addr(master), _addr(m),
+    _check_step(grads, grad_dtype, psi_pad, _state("", master, m, v, w_bf16))
+    _check(result, 16, "result")
+    return _lib.zero_step_noalloc(_grad_array(grads, N), grad_dtype, _addr(master), _addr(m),
                                   _addr(v), _addr(w_bf16), psi_pad, N, ctypes.byref(hp),
                                   loss_scale, _addr(result), _stream(stream))
 
@@ -306,7 +367,12 @@ def zero_step_noalloc(grads, grad_dtype: int, master, m, v, w_bf16, psi_pad: int
 def zero3_gather(shards, N: int, shard: int, begin: int, end: int, view, stream=None,
                  flags: int = 0) -> int:
     """Elements [begin, end) of the full BF16 view, gathered from N shards."""
-    arr = (ctypes.c_void_p * max(len(shards), 1))(*[_addr(x) for x in shards])
+    # sizes the library refuses are left for it to refuse
+    if 1 <= N <= ZERO_MAX_RANKS and 0 < shard <= ZERO_MAX_ELEMS // N and 0 <= begin < end <= N * shard:
+        for i, t in enumerate(shards):
+            _check(t, 2 * shard, f"shards[{i}]")
+        _check(view, 2 * (end - begin), "view")
+    arr = _grad_array(shards, N)
     return _lib.zero3_gather(arr, N, shard, begin, end, _addr(view), flags, _stream(stream))
 
 
