@@ -412,7 +412,10 @@ def run_ours(args, world, rank, local):
                    out_of_place=out_of_place, device=dev, master=master,
                    micro_batches=args.micro_batches, host_grad_accum=args.host_grad_accum,
                    device_policy=device_policy, pingpong=pingpong,
-                   smem_staging=Z.ZERO_STAGING_TMA if args.staging == "tma" else 0)
+                   smem_staging=Z.ZERO_STAGING_TMA if args.staging == "tma" else 0,
+                   # a captured step reads its bias corrections from a table
+                   policy_table_steps=(args.warmup + args.steps + 64
+                                       if args.profile_graph and device_policy else 0))
     buckets = opt.bucket_bounds()
     k_micro = max(1, args.micro_batches)
     # One event pair per step around its sequence of first-pass launches.
@@ -450,22 +453,15 @@ def run_ours(args, world, rank, local):
         one_step(k)
     torch.cuda.synchronize(dev)
     if args.profile_graph:
-        # One more step, captured as a graph and replayed once inside the
-        # profiler range (once only: the captured prologue holds a window of one
-        # t).  Capturing runs nothing and changes no host state here: with the
-        # device policy and ping-pong sets, t, the loss scale and the current
-        # set all live on the device.
+        # One more step, captured as a graph (ZeroAdam.capture_step) and
+        # replayed once inside the profiler range.  Capturing runs nothing:
+        # with the device policy, its table and ping-pong sets, t, the loss
+        # scale, the bias corrections and the current set all live on the
+        # device.
         if not (device_policy and pingpong and k_micro == 1):
             raise SystemExit("--profile-graph needs the device policy and ping-pong sets")
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(graph, stream=cap, capture_error_mode="relaxed"):
-            opt.enqueue(grads, cap, api=args.api)
+        graph = opt.capture_step(grads)
         torch.cuda.synchronize(dev)
-        # every step noted as in flight has completed, and the one noted while
-        # capturing was never recorded on a running stream: forget them all
-        opt._inflight.clear()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.profiler.start()
         g0.record(stream)

@@ -305,6 +305,11 @@ typedef struct {
     int32_t rows_used;                 /* rows handed out in the current step             */
     int32_t row_width;                 /* slots of the latest row that count               */
     int32_t shared_slots_used;         /* 1 once a launch of the step had no row of its own */
+    const float* policy_table;         /* device policy: the device address of the caller's
+                                          table of bias corrections
+                                          (zero_plan_set_device_policy_table); NULL (as
+                                          zero_plan_init leaves it) = the window passed
+                                          with the launch                                 */
 } zero_plan;
 
 /* Values of zero_plan.smem_staging.
@@ -410,6 +415,35 @@ typedef struct {
  * zero_plan_begin.  Returns ZERO_OK or ZERO_ERR_ARG. */
 int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* policy, int64_t t_first,
                                 int32_t t_count);
+
+/* The bias corrections of a device policy for t = t_first .. t_first +
+ * t_count - 1, two floats per t: table[2*i] = lr / (1 - beta1^t) and
+ * table[2*i + 1] = sqrt(1 - beta2^t) for t = t_first + i, each rounded once
+ * to FP32 from FP64, exactly as a step with hp->step = t rounds them.
+ *   hp       host pointer to the hyper-parameters the steps will use (lr,
+ *            beta1 and beta2 enter the table)
+ *   table    host array of 2 * t_count floats, written on success
+ * t_first >= 1, 1 <= t_count and t_first + t_count - 1 <= ZERO_MAX_ELEMS.
+ * Returns ZERO_OK or ZERO_ERR_ARG (nothing written).  Host only. */
+int zero_policy_table_fill(const zero_adam_hparams* hp, int64_t t_first, int64_t t_count,
+                           float* table);
+
+/* zero_plan_set_device_policy with the bias corrections read from a table
+ * instead of a window passed with the launch.  table holds 2 * t_count
+ * floats filled by zero_policy_table_fill(hp, t_first, t_count, ...) with the
+ * plan's lr and betas; it is caller-owned, device-addressable (device memory,
+ * or pinned host memory), 8-byte aligned, and must stay unchanged while
+ * steps that read it are in flight; 1 <= t_count.  The step reads the entry of
+ * t' = policy->t + 1; a t' outside [t_first, t_first + t_count) ends the step
+ * with ZERO_ERR_POLICY_WINDOW and changes nothing, as with a window.
+ * The launches then carry no value that depends on t, so a step captured in
+ * a CUDA graph (its gradients, state sets and policy at fixed addresses) can
+ * be replayed once per step for every t the table covers, with t, the loss
+ * scale and, with ping-pong sets, the current set all kept on the device.
+ * Call between zero_plan_init(_ex) and zero_plan_begin.  Returns ZERO_OK or
+ * ZERO_ERR_ARG. */
+int zero_plan_set_device_policy_table(zero_plan* plan, zero_device_policy* policy,
+                                      const float* table, int64_t t_first, int32_t t_count);
 
 /* ------------------------------------------------------------------------
  * Ping-pong state sets.  An out-of-place step reads one full set of

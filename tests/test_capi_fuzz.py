@@ -36,7 +36,7 @@ def _no_gpu() -> bool:
 pytestmark = pytest.mark.skipif(not _no_gpu(), reason="made-up addresses: host-only test")
 
 CHILD = r'''
-import json, random, sys
+import ctypes, json, random, sys
 sys.path.insert(0, ROOT)
 from zero_sharded_mixed_04_gb300 import zero as Z
 GB = 1 << 30
@@ -79,7 +79,7 @@ def case(seed):
         ws_bytes = r.choice([need, max(0, need - 1), 0, need + (1 << 20), 16640])
         ls = r.choice([1.0, 0.0, -1.0, float("inf"), float("nan"), 65536.0])
         which = r.choice(["step", "into", "plan", "noalloc", "ws", "layout", "ledger",
-                          "gather", "peak", "comm"])
+                          "gather", "peak", "comm", "table"])
         if which == "step":
             rc = Z.zero_step(base, dtype, *st, psi_pad, N, hp, ls, ws, ws_bytes, None, 0)
         elif which == "into":
@@ -95,6 +95,11 @@ def case(seed):
                 # a begin are refused on the host
                 rc2 = Z.zero_plan_bucket(plan, 0, max(8, psi_pad), None, 0)
                 rc3 = Z.zero_plan_end(plan, None, 0)
+                # made-up policy and table addresses: no device maps them
+                rc4 = Z.zero_plan_set_device_policy_table(plan, 9 * GB, 9 * GB + 4096,
+                                                          r.choice([1, 0, MAXE]),
+                                                          r.choice([1, 64, 0, -1]))
+                out.append(["plan_policy_table", rc4])
                 rc = Z.zero_plan_begin(plan, 0)
                 out.append(["plan_bucket_before_begin", rc2])
                 out.append(["plan_end_before_begin", rc3])
@@ -118,6 +123,16 @@ def case(seed):
             layers = [r.choice([0, 1, 1 << 20, -1, MAXE, 1 << 62]) for _ in range(r.randrange(0, 5))]
             v = Z.zero3_peak_bytes(layers, N)
             rc = "neg1" if v == -1 else ("ok" if v >= 0 else "negative")
+        elif which == "table":
+            # the table is written: a real buffer for the counts the library
+            # may accept, a made-up address only for counts it must refuse
+            t_first = r.choice([-1, 0, 1, 5, MAXE, MAXE + 1, 1 << 62])
+            t_count = r.choice([-1, 0, 1, 7, MAXE + 1, 1 << 62, -(1 << 63)])
+            if 1 <= t_count <= 7:
+                buf = (ctypes.c_float * (2 * t_count))()
+                rc = Z.zero_policy_table_fill(hp, t_first, t_count, ctypes.addressof(buf))
+            else:
+                rc = Z.zero_policy_table_fill(hp, t_first, t_count, 7 * GB)
         else:
             shard = size(r, 8)
             rc = Z.zero3_gather(base, N, shard, r.choice([0, 5, -1, 8]),
@@ -131,7 +146,8 @@ print(json.dumps(case(int(sys.argv[1]))))
 ALLOWED = {
     "step": {0, -1, -2, -3, -5, -6, 1}, "into": {0, -1, -2, -3, -5, -6, 1},
     "noalloc": {0, -1, -2, -3, -5, -6, -7, 1}, "plan": {0, -1, -2, -3, -5, -6},
-    "plan_bucket_before_begin": {-1}, "plan_end_before_begin": {-1},
+    "plan_bucket_before_begin": {-1}, "plan_end_before_begin": {-1}, "plan_policy_table": {-1},
+    "table": {0, -1},
     "ws": {"zero", "ok"}, "layout": {0, -1}, "ledger": {"neg1", "ok"},
     "comm": {"neg1", "ok"}, "peak": {"neg1", "ok"}, "gather": {0, -1, -2, -3, -6},
 }

@@ -538,3 +538,40 @@ def test_binding_refuses_tensors_too_small_for_the_call(zero_lib):
     small = torch.zeros(8, dtype=torch.int16)
     assert Z.zero3_gather([small] * N, N, 1024, 0, 4097, small, 0, 0) == Z.ZERO_ERR_ARG
     assert Z.zero_plan_bucket(plan, 0, n + 512, [small] * N, 0) == Z.ZERO_ERR_ARG
+
+
+@pytest.mark.parametrize("lr,beta1,beta2", [(1e-3, 0.9, 0.999), (3e-4, 0.8, 0.95),
+                                            (1e-2, 0.0, 0.0), (0.1, 0.999, 0.99999)])
+def test_policy_table_matches_the_oracle_scalars(zero_lib, oracle_mod, lr, beta1, beta2):
+    """Every entry of a device-policy table is the oracle's FP32 step_size and
+    sqrt(1 - beta2^t) for its t, bit for bit, from t = 1 into the range where
+    the bias corrections reach 1."""
+    Z = zero_lib
+    hp = Z.make_hparams(lr=lr, beta1=beta1, beta2=beta2, step=7)
+    ohp = oracle_mod.Hparams(lr=lr, beta1=beta1, beta2=beta2)
+    for t_first, t_count in ((1, 300), (999_990, 20), ((1 << 31) - 4, 3)):
+        table = (ctypes.c_float * (2 * t_count))()
+        assert Z.zero_policy_table_fill(hp, t_first, t_count, ctypes.addressof(table)) == Z.ZERO_OK
+        for i in range(t_count):
+            s = oracle_mod.step_scalars(ohp, t_first + i, 4, 1.0)
+            want = np.array([s["step_size"], s["sbc2"]], np.float32)
+            got = np.array([table[2 * i], table[2 * i + 1]], np.float32)
+            assert got.tobytes() == want.tobytes(), (t_first + i, got, want)
+    assert hp.step == 7  # the caller's hyper-parameters are left alone
+
+
+def test_policy_table_rejects_bad_arguments(zero_lib):
+    Z = zero_lib
+    hp = Z.make_hparams()
+    table = (ctypes.c_float * 8)()
+    a = ctypes.addressof(table)
+    for t_first, t_count in ((0, 1), (1, 0), (-5, 2), (1, -1), (Z.ZERO_MAX_ELEMS, 2),
+                             (2, Z.ZERO_MAX_ELEMS)):
+        assert Z.zero_policy_table_fill(hp, t_first, t_count, a) == Z.ZERO_ERR_ARG
+    assert Z.zero_policy_table_fill(hp, 1, 1, None) == Z.ZERO_ERR_ARG
+    assert Z.zero_policy_table_fill(Z.make_hparams(beta2=1.0), 1, 1, a) == Z.ZERO_ERR_ARG
+    assert list(table) == [0.0] * 8
+    assert Z.zero_policy_table_fill(hp, Z.ZERO_MAX_ELEMS, 1, a) == Z.ZERO_OK
+    # a plan that has not been initialised takes no table
+    plan = Z.zero_plan()
+    assert Z.zero_plan_set_device_policy_table(plan, a, a, 1, 4) == Z.ZERO_ERR_ARG

@@ -1038,12 +1038,14 @@ struct PolicyTable {
 //   - Ping-pong sets: snapshots which set is current into the control block,
 //     where every kernel of the step reads it.
 //   - Device policy: picks the scalars for t' = policy->t + 1 from the host's
-//     window, forms the batch-mean factor from the device's loss scale, and
-//     leaves them in the control block for the step's kernels.
+//     window (the launch's `window`), or from the caller's table in memory
+//     (`table`: step_size and sbc2 for each t, in pairs), forms the
+//     batch-mean factor from the device's loss scale, and leaves them in the
+//     control block for the step's kernels.
 __global__ void zero_step_prologue_kernel(const zero_device_policy* policy, Ctrl* ctrl,
-                                          Scalars base, PolicyTable table, int64_t t_first,
-                                          int32_t t_count, double ranks_times_micro,
-                                          const int32_t* current_set) {
+                                          Scalars base, PolicyTable window, const float* table,
+                                          int64_t t_first, int64_t t_count,
+                                          double ranks_times_micro, const int32_t* current_set) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     if (current_set != nullptr)
         ctrl->cur = *reinterpret_cast<const volatile int32_t*>(current_set) != 0 ? 1 : 0;
@@ -1052,9 +1054,12 @@ __global__ void zero_step_prologue_kernel(const zero_device_policy* policy, Ctrl
     Scalars s = base;
     if (idx < 0 || idx >= t_count) {
         ctrl->policy_error = 1;  // every kernel of the step then leaves the state alone
+    } else if (table != nullptr) {
+        s.step_size = table[2 * idx];
+        s.sbc2 = table[2 * idx + 1];
     } else {
-        s.step_size = table.step_size[idx];
-        s.sbc2 = table.sbc2[idx];
+        s.step_size = window.step_size[idx];
+        s.sbc2 = window.sbc2[idx];
     }
     s.inv = static_cast<float>(1.0 / (ranks_times_micro * static_cast<double>(policy->loss_scale)));
     ctrl->scalars = s;

@@ -510,19 +510,26 @@ int plan_begin(zero_plan* p, void* stream) {
         cudaSuccess)
         return ZERO_ERR_CUDA;
     if (p->policy != nullptr || p->current_set != nullptr) {
-        PolicyTable table{};
-        zero_adam_hparams hp = p->hp;
-        for (int32_t i = 0; i < p->policy_t_count; ++i) {
-            hp.step = p->policy_t_first + i;
-            const Scalars si = make_scalars(&hp, p->N, p->loss_scale);
-            table.step_size[i] = si.step_size;
-            table.sbc2[i] = si.sbc2;
+        // the window of bias corrections travels with the launch, unless the
+        // plan reads them from the caller's table
+        PolicyTable window{};
+        if (p->policy_table == nullptr) {
+            zero_adam_hparams hp = p->hp;
+            const int32_t n = p->policy_t_count < ZERO_POLICY_WINDOW ? p->policy_t_count
+                                                                      : ZERO_POLICY_WINDOW;
+            for (int32_t i = 0; i < n; ++i) {
+                hp.step = p->policy_t_first + i;
+                const Scalars si = make_scalars(&hp, p->N, p->loss_scale);
+                window.step_size[i] = si.step_size;
+                window.sbc2[i] = si.sbc2;
+            }
         }
         const Scalars base = make_scalars(&p->hp, p->N, p->loss_scale);
         zero_step_prologue_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
             static_cast<const zero_device_policy*>(p->policy),
-            reinterpret_cast<Ctrl*>(p->workspace), base, table, p->policy_t_first,
-            p->policy_t_count, static_cast<double>(p->N) * micro_batches_of(&p->hp),
+            reinterpret_cast<Ctrl*>(p->workspace), base, window, p->policy_table,
+            p->policy_t_first, p->policy_t_count,
+            static_cast<double>(p->N) * micro_batches_of(&p->hp),
             static_cast<const int32_t*>(p->current_set));
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (cudaGetLastError() != cudaSuccess) return ZERO_ERR_CUDA;
@@ -792,23 +799,68 @@ extern "C" int zero_plan_init_ex(zero_plan* plan, const void* const* grads, int3
                      workspace_bytes_given, true, grad_accum);
 }
 
+namespace {
+
+// The device address of a device-addressable buffer (device memory, or pinned
+// host memory mapped for the device), or nullptr.
+void* device_address(const void* p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess || attr.devicePointer == nullptr) {
+        cudaGetLastError();  // clear the error that query may leave behind
+        return nullptr;
+    }
+    return attr.devicePointer;
+}
+
+int set_device_policy(zero_plan* plan, zero_device_policy* policy, const float* table,
+                      int64_t t_first, int32_t t_count) {
+    // An in-place one-pass step cannot leave its state alone once it has run,
+    // so a window miss must be caught before: only the plan's kernels check
+    // it, and they all do.
+    void* pol = device_address(policy);
+    if (pol == nullptr) return ZERO_ERR_ARG;
+    const void* tab = nullptr;
+    if (table != nullptr && (tab = device_address(table)) == nullptr) return ZERO_ERR_ARG;
+    plan->policy = pol;
+    plan->policy_table = static_cast<const float*>(tab);
+    plan->policy_t_first = t_first;
+    plan->policy_t_count = t_count;
+    return ZERO_OK;
+}
+
+}  // namespace
+
 extern "C" int zero_plan_set_device_policy(zero_plan* plan, zero_device_policy* policy,
                                            int64_t t_first, int32_t t_count) {
     if (plan == nullptr || plan->state != 1 || policy == nullptr || t_first < 1 || t_count < 1 ||
         t_count > ZERO_POLICY_WINDOW || !aligned(policy, 8))
         return ZERO_ERR_ARG;
-    // An in-place one-pass step cannot leave its state alone once it has run,
-    // so a window miss must be caught before: only the plan's kernels check
-    // it, and they all do.  The policy must be device-addressable.
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, policy) != cudaSuccess || attr.devicePointer == nullptr) {
-        cudaGetLastError();
+    return set_device_policy(plan, policy, nullptr, t_first, t_count);
+}
+
+extern "C" int zero_policy_table_fill(const zero_adam_hparams* hp, int64_t t_first,
+                                      int64_t t_count, float* table) {
+    if (table == nullptr || !valid_hparams(hp) || t_first < 1 || t_count < 1 ||
+        t_count > ZERO_MAX_ELEMS || t_first - 1 > ZERO_MAX_ELEMS - t_count)
         return ZERO_ERR_ARG;
+    zero_adam_hparams h = *hp;
+    for (int64_t i = 0; i < t_count; ++i) {
+        h.step = t_first + i;
+        const Scalars s = make_scalars(&h, 1, 1.0f);
+        table[2 * i] = s.step_size;
+        table[2 * i + 1] = s.sbc2;
     }
-    plan->policy = attr.devicePointer;
-    plan->policy_t_first = t_first;
-    plan->policy_t_count = t_count;
     return ZERO_OK;
+}
+
+extern "C" int zero_plan_set_device_policy_table(zero_plan* plan, zero_device_policy* policy,
+                                                 const float* table, int64_t t_first,
+                                                 int32_t t_count) {
+    if (plan == nullptr || plan->state != 1 || policy == nullptr || table == nullptr ||
+        t_first < 1 || t_count < 1 || t_first - 1 > ZERO_MAX_ELEMS - t_count ||
+        !aligned(policy, 8) || !aligned(table, 8))
+        return ZERO_ERR_ARG;
+    return set_device_policy(plan, policy, table, t_first, t_count);
 }
 
 extern "C" int zero_plan_set_pingpong(zero_plan* plan, int32_t* current_set) {

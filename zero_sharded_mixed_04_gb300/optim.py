@@ -68,7 +68,7 @@ class ZeroAdam:
                  dynamic_loss_scale=False, growth_interval=2000, out_of_place=False,
                  device="cuda", master: torch.Tensor | None = None, micro_batches: int = 0,
                  host_grad_accum: bool = False, device_policy: bool = False,
-                 smem_staging: int = 0, pingpong: bool = False):
+                 smem_staging: int = 0, pingpong: bool = False, policy_table_steps: int = 0):
         if pingpong and not out_of_place:
             raise ValueError("ping-pong state sets need the out-of-place step")
         self.psi_pad, self.N = psi_pad, N
@@ -123,6 +123,18 @@ class ZeroAdam:
             self.policy.backoff = self.scaler.backoff
             self.policy.growth = self.scaler.growth
             self._inflight = collections.deque()
+        # policy_table_steps: the bias corrections of t = 1 .. policy_table_steps
+        # sit in a device table (zero_plan_set_device_policy_table) instead of
+        # travelling with each launch, so no launch depends on t and a captured
+        # step can be replayed (capture_step); lr and the betas are fixed then
+        self.policy_table = None
+        if policy_table_steps > 0:
+            if not device_policy:
+                raise ValueError("a policy table needs the device policy")
+            host = torch.empty(2 * policy_table_steps, dtype=torch.float32)
+            Z.check(Z.zero_policy_table_fill(self.hp, 1, policy_table_steps, host),
+                    "zero_policy_table_fill")
+            self.policy_table = host.to(self.device)
         self.result_t = torch.zeros(4, dtype=torch.int32, pin_memory=True)
         self.last = None
         # pingpong: the device-kept index of the current set, in pinned memory
@@ -344,13 +356,18 @@ class ZeroAdam:
     def _apply_policy(self, plan, stream) -> None:
         if self.pingpong:
             Z.check(Z.zero_plan_set_pingpong(plan, self.set_mem), "zero_plan_set_pingpong")
-        if self.policy_mem is not None:
+        if self.policy_table is not None:
+            Z.check(Z.zero_plan_set_device_policy_table(plan, self.policy_mem, self.policy_table,
+                                                        1, self.policy_table.numel() // 2),
+                    "zero_plan_set_device_policy_table")
+        elif self.policy_mem is not None:
             t_first, t_count = self._policy_window(stream)
             Z.check(Z.zero_plan_set_device_policy(plan, self.policy_mem, t_first, t_count),
                     "zero_plan_set_device_policy")
 
     def _note_enqueued(self, s) -> None:
-        if self.policy_mem is not None:
+        # only a window of bias corrections depends on how many steps are in flight
+        if self.policy_mem is not None and self.policy_table is None:
             ev = torch.cuda.Event()
             ev.record(s)
             self._inflight.append(ev)
@@ -428,6 +445,30 @@ class ZeroAdam:
         self.enqueue(grads, stream, api, bucket_events, span_events)
         return self.finish(stream)
 
+
+    # ---------------------------------------------------------------- CUDA graphs
+    def capture_step(self, grads, stream=None) -> torch.cuda.CUDAGraph:
+        """One step on ``grads`` (N device buffers) captured as a CUDA graph.
+        Each replay runs one more step with whatever the buffers then hold:
+        refill them on the replaying stream, then replay.  The step keeps all
+        of its host state on the device (t, the loss scale, the bias
+        corrections from the policy table and, out of place, the current
+        ping-pong set), so replays need no host work in between; the host
+        catches up at finish_pending() or state().  Needs the device policy
+        with a policy table, and ping-pong sets when out of place."""
+        if self.policy_table is None:
+            raise ValueError("capture_step needs device_policy and policy_table_steps")
+        if self.out_of_place and not self.pingpong:
+            raise ValueError("capture_step needs ping-pong sets when out of place")
+        if self.hp.micro_batches > 1:
+            raise ValueError("capture_step takes one batch")
+        s = stream if stream is not None else torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        graph = torch.cuda.CUDAGraph()
+        # relaxed: the plan queries pointer attributes while it is captured
+        with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+            self._enqueue_plan(grads, None, s, None)
+        return graph
 
     # ---------------------------------------------------------------- checkpoint
     def finish_pending(self) -> None:

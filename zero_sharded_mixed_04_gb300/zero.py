@@ -95,7 +95,8 @@ class zero_plan(ctypes.Structure):
                 ("smem_staging", ctypes.c_int32), ("current_set", ctypes.c_void_p),
                 ("rows_offset", ctypes.c_int64), ("row_capacity", ctypes.c_int32),
                 ("rows_used", ctypes.c_int32), ("row_width", ctypes.c_int32),
-                ("shared_slots_used", ctypes.c_int32)]
+                ("shared_slots_used", ctypes.c_int32),
+                ("policy_table", ctypes.c_void_p)]
 
 
 class zero_device_policy(ctypes.Structure):
@@ -131,6 +132,10 @@ _lib.zero_plan_init_ex.argtypes = [_PLAN, _P, _i32, _P, _P, _P, _P, _P, _P, _P, 
 _lib.zero_plan_init_ex.restype = ctypes.c_int
 _lib.zero_plan_set_device_policy.argtypes = [_PLAN, _P, _i64, _i32]
 _lib.zero_plan_set_device_policy.restype = ctypes.c_int
+_lib.zero_policy_table_fill.argtypes = [ctypes.POINTER(zero_adam_hparams), _i64, _i64, _P]
+_lib.zero_policy_table_fill.restype = ctypes.c_int
+_lib.zero_plan_set_device_policy_table.argtypes = [_PLAN, _P, _P, _i64, _i32]
+_lib.zero_plan_set_device_policy_table.restype = ctypes.c_int
 _lib.zero_plan_set_pingpong.argtypes = [_PLAN, _P]
 _lib.zero_plan_set_pingpong.restype = ctypes.c_int
 _lib.zero_plan_begin.argtypes = [_PLAN, _P]
@@ -325,6 +330,23 @@ def zero_plan_set_device_policy(plan: zero_plan, policy, t_first: int, t_count: 
     return _lib.zero_plan_set_device_policy(ctypes.byref(plan), _addr(policy), t_first, t_count)
 
 
+def zero_policy_table_fill(hp: zero_adam_hparams, t_first: int, t_count: int, table) -> int:
+    """table: a host buffer of 2 * t_count floats (a CPU tensor or an address)."""
+    if t_count > 0:
+        _check(table, 8 * t_count, "table")
+    return _lib.zero_policy_table_fill(ctypes.byref(hp), t_first, t_count, _addr(table))
+
+
+def zero_plan_set_device_policy_table(plan: zero_plan, policy, table, t_first: int,
+                                      t_count: int) -> int:
+    """policy as for zero_plan_set_device_policy; table: a device-addressable
+    buffer of 2 * t_count floats filled by zero_policy_table_fill."""
+    if t_count > 0:
+        _check(table, 8 * t_count, "table")
+    return _lib.zero_plan_set_device_policy_table(ctypes.byref(plan), _addr(policy), _addr(table),
+                                                  t_first, t_count)
+
+
 def zero_plan_set_pingpong(plan: zero_plan, current_set) -> int:
     """current_set: the address of a device-addressable int32 (a pinned host
     tensor or a device tensor) naming the current state set, 0 or 1."""
@@ -408,7 +430,8 @@ def exported_symbols() -> list[str]:
     """Names of the C functions this binding expects the library to export."""
     return ["zero_init_layout", "zero_shard_range", "zero_workspace_bytes", "zero_step",
             "zero_step_into", "zero_plan_init", "zero_plan_init_ex",
-            "zero_plan_set_device_policy", "zero_plan_set_pingpong", "zero_plan_begin",
+            "zero_plan_set_device_policy", "zero_policy_table_fill",
+            "zero_plan_set_device_policy_table", "zero_plan_set_pingpong", "zero_plan_begin",
             "zero_plan_bucket",
             "zero_plan_end", "zero_ledger", "zero_comm_volume", "zero_status_str",
             "zero_launch_count", "zero_step_noalloc", "zero3_gather", "zero3_peak_bytes",
