@@ -60,6 +60,11 @@ class ZeroAdam:
     (``zero_plan_set_pingpong``): a skipped step then leaves the current set
     current instead of copying it into the other one.  The host learns the
     current set when it next synchronises (``state()`` does).
+
+    ``device_policy`` keeps t and the loss scale on the device, so steps need
+    no host read in between.  With ``policy_table_steps`` = T as well, the bias
+    corrections of t = 1 .. T come from a device table, no launch depends on
+    t, and ``capture_step`` records one step as a CUDA graph to replay.
     """
 
     def __init__(self, psi_pad: int, N: int, grad_dtype: str = "bf16", *, lr=1e-3, beta1=0.9,
