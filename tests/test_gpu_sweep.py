@@ -13,7 +13,8 @@ in combinations no hand-written case lists:
   - one bucket or many, the zero_step or plan entry points, the register or
     the TMA-staged kernel;
   - one batch or 2-3 accumulated micro-batches;
-  - a +inf, -inf or NaN planted in some step, micro-batch, rank and element.
+  - a +inf, -inf or NaN planted in some step, micro-batch, rank and element;
+  - eager steps, or one step captured as a CUDA graph and replayed.
 Each case runs three steps through ZeroAdam (the library's public Python API)
 and compares every step's outcome and state with the oracle: bit for bit
 without clip, within the clip tolerance with it.  A failing case names its
@@ -69,6 +70,11 @@ def draw_case(seed: int) -> dict:
         else r.choice(["step", "plan"]),
         "loss_scale": r.choice([1.0, 128.0, 4096.0]), "sigma": r.choice([1e-4, 1e-3, 3e-2]),
         "bad": bad,
+        # drawn last, so that the other options of every seed stay as they were:
+        # the step captured once as a CUDA graph and replayed (device policy
+        # with a table of bias corrections; in place or with ping-pong sets)
+        "graph": (device_policy and k == 1 and (pingpong or not out_of_place)
+                  and r.random() < 0.5),
     }
 
 
@@ -104,7 +110,13 @@ def run_case(case: dict, oracle_mod) -> None:
                    out_of_place=case["out_of_place"], device=dev, master=master.to(dev),
                    micro_batches=case["k"] if case["k"] > 1 else 0,
                    device_policy=case["device_policy"], smem_staging=case["staging"],
-                   pingpong=case["pingpong"])
+                   pingpong=case["pingpong"],
+                   policy_table_steps=STEPS + 4 if case.get("graph") else 0)
+    graph, bufs = None, None
+    if case.get("graph"):
+        tdt = torch.bfloat16 if case["dtype"] == "bf16" else torch.float32
+        bufs = [torch.zeros(psi_pad, dtype=tdt, device=dev) for _ in range(case["N"])]
+        graph = opt.capture_step(bufs)
     ref = {"master": master.numpy().copy(), "m": np.zeros(psi_pad, np.float32),
            "v": np.zeros(psi_pad, np.float32), "w": np.zeros(psi_pad, np.uint16)}
     hp = oracle_mod.Hparams(lr=case["lr"], beta1=case["beta1"], beta2=case["beta2"],
@@ -122,7 +134,14 @@ def run_case(case: dict, oracle_mod) -> None:
                                               ref["master"], ref["m"], ref["v"], ref["w"], hp,
                                               o_t + 1, o_scale, case["skip"])
         else:
-            res = opt.step([g.to(dev) for g in micro[0]], api=case["api"])
+            if graph is not None:
+                for b, g in zip(bufs, micro[0]):
+                    b.copy_(g)
+                graph.replay()
+                torch.cuda.synchronize(dev)
+                res = opt.last_result()
+            else:
+                res = opt.step([g.to(dev) for g in micro[0]], api=case["api"])
             ores = oracle_mod.zero_step([_np(g) for g in micro[0]], ref["master"], ref["m"],
                                         ref["v"], ref["w"], hp, o_t + 1, o_scale, case["skip"])
         tag = f"case {case}, step {step}: "
@@ -135,6 +154,8 @@ def run_case(case: dict, oracle_mod) -> None:
         if case["dynamic"]:
             o_scale, o_good = oracle_mod.loss_scale_update(o_scale, o_good,
                                                            ores["found_nonfinite"], 2, 0.5, 2.0)
+        if graph is not None:
+            opt.finish_pending()  # the host's t and scale catch up with the device's
         assert opt.t == o_t and opt.scaler.scale == o_scale, tag
         compare_state(state_to_numpy(opt.state()), ref, exact, tag=tag)
 
@@ -159,4 +180,9 @@ def test_sweep_covers_the_options():
     assert any(c["bad"] is not None and c["skip"] for c in cases)
     assert any(c["bad"] is not None and not c["skip"] for c in cases)
     assert any(c["k"] > 1 and c["staging"] and not c["out_of_place"] for c in cases)
+    graphs = [c for c in cases if c["graph"]]
+    assert len(graphs) >= 10
+    assert {c["out_of_place"] for c in graphs} == {False, True}
+    assert {c["staging"] for c in graphs} == {0, 1} and {c["dtype"] for c in graphs} == {"bf16", "fp32"}
+    assert any(c["bad"] is not None for c in graphs) and any(c["clip"] > 0 for c in graphs)
     assert sum(c["psi_pad"] > 1 << 22 for c in cases) >= 8
