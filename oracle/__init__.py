@@ -85,15 +85,15 @@ def _declare(lib):
     lib.orc_ledger_bytes.restype = i64
     lib.orc_comm_volume.argtypes = [i64, i32, i32, i32]
     lib.orc_comm_volume.restype = i64
-    lib.orc_step_scalars.argtypes = [P, i32, i32, f64, P]
+    lib.orc_step_scalars.argtypes = [P, i64, i32, f64, P]
     lib.orc_reduce_scatter.argtypes = [P, i32, i32, i64, i32, f32, P]
     lib.orc_all_reduce.argtypes = [P, i32, i32, i64, f32, P]
     lib.orc_all_gather_f32.argtypes = [P, i32, i64, P]
-    lib.orc_zero_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
+    lib.orc_zero_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i64, f64, i32, P]
     lib.orc_zero_step.restype = i32
-    lib.orc_ddp_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64, i32, P]
+    lib.orc_ddp_step.argtypes = [P, i32, i32, i64, P, P, P, P, P, i64, f64, i32, P]
     lib.orc_ddp_step.restype = i32
-    lib.orc_zero_step_accum.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, i32, f64,
+    lib.orc_zero_step_accum.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, i64, f64,
                                          i32, P]
     lib.orc_zero_step_accum.restype = i32
     lib.orc_gather_range.argtypes = [P, i32, i64, i64, i64, P]
@@ -101,7 +101,7 @@ def _declare(lib):
     lib.orc_zero3_peak_bytes.argtypes = [P, i64, i32, i32, i32]
     lib.orc_zero3_peak_bytes.restype = i64
     lib.orc_check_accumulate.argtypes = [P, i32, i32, i64, f32, P, P]
-    lib.orc_step_window.argtypes = [P, i32, i32, i64, P, P, P, P, P, i32, f64,
+    lib.orc_step_window.argtypes = [P, i32, i32, i64, P, P, P, P, P, i64, f64,
                                     i32, i32, f32]
     lib.orc_clip_coef_from_sumsq.argtypes = [f64, f64]
     lib.orc_clip_coef_from_sumsq.restype = f32

@@ -255,7 +255,7 @@ typedef struct {
 
 /* Each scalar is formed in FP64 from the FP64 hyper-parameters and rounded
  * once to FP32.  t is the 1-based count of applied steps including this one. */
-void orc_step_scalars(const orc_hparams* hp, int32_t t, int32_t N,
+void orc_step_scalars(const orc_hparams* hp, int64_t t, int32_t N,
                       double loss_scale, orc_scalars* s)
 {
     s->inv = (float)(1.0 / ((double)N * loss_scale));
@@ -422,7 +422,7 @@ typedef struct {
  * holds [r*S, (r+1)*S).  Returns 0, or -1 on a bad argument or no memory. */
 int orc_zero_step(const void* const* grads, int32_t dtype, int32_t N, int64_t psi_pad,
                   float* master, float* m, float* v, uint16_t* w,
-                  const orc_hparams* hp, int32_t t, double loss_scale,
+                  const orc_hparams* hp, int64_t t, double loss_scale,
                   int32_t skip_on_overflow, orc_result* res)
 {
     if (N < 1 || psi_pad < 0 || psi_pad % ((int64_t)N * ORC_PAD_UNIT) != 0)
@@ -482,7 +482,7 @@ int orc_zero_step(const void* const* grads, int32_t dtype, int32_t N, int64_t ps
  * exactly this state ([RC-T2 N48]: all ranks still train one model). */
 int orc_ddp_step(const void* const* grads, int32_t dtype, int32_t N, int64_t psi_pad,
                  float* const* master, float* const* m, float* const* v,
-                 uint16_t* const* w, const orc_hparams* hp, int32_t t,
+                 uint16_t* const* w, const orc_hparams* hp, int64_t t,
                  double loss_scale, int32_t skip_on_overflow, orc_result* res)
 {
     if (N < 1 || psi_pad < 0 || psi_pad % ((int64_t)N * ORC_PAD_UNIT) != 0)
@@ -539,7 +539,7 @@ int orc_ddp_step(const void* const* grads, int32_t dtype, int32_t N, int64_t psi
 /* grads holds k * N pointers, micro-batch major: grads[mb * N + r]. */
 int orc_zero_step_accum(const void* const* grads, int32_t dtype, int32_t N, int32_t k,
                         int64_t psi_pad, float* master, float* m, float* v, uint16_t* w,
-                        const orc_hparams* hp, int32_t t, double loss_scale,
+                        const orc_hparams* hp, int64_t t, double loss_scale,
                         int32_t skip_on_overflow, orc_result* res)
 {
     if (N < 1 || k < 1 || psi_pad < 0 || psi_pad % ((int64_t)N * ORC_PAD_UNIT) != 0)
@@ -612,7 +612,7 @@ void orc_check_accumulate(const void* const* grads, int32_t dtype, int32_t N,
  * window are updated. */
 void orc_step_window(const void* const* grads, int32_t dtype, int32_t N, int64_t n,
                      float* master, float* m, float* v, uint16_t* w,
-                     const orc_hparams* hp, int32_t t, double loss_scale,
+                     const orc_hparams* hp, int64_t t, double loss_scale,
                      int32_t apply, int32_t clip, float clip_coef)
 {
     if (!apply)

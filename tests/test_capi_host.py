@@ -545,11 +545,11 @@ def test_binding_refuses_tensors_too_small_for_the_call(zero_lib):
 def test_policy_table_matches_the_oracle_scalars(zero_lib, oracle_mod, lr, beta1, beta2):
     """Every entry of a device-policy table is the oracle's FP32 step_size and
     sqrt(1 - beta2^t) for its t, bit for bit, from t = 1 into the range where
-    the bias corrections reach 1."""
+    the bias corrections reach 1, and across 2^31 (t is 64-bit on both sides)."""
     Z = zero_lib
     hp = Z.make_hparams(lr=lr, beta1=beta1, beta2=beta2, step=7)
     ohp = oracle_mod.Hparams(lr=lr, beta1=beta1, beta2=beta2)
-    for t_first, t_count in ((1, 300), (999_990, 20), ((1 << 31) - 4, 3)):
+    for t_first, t_count in ((1, 300), (999_990, 20), ((1 << 31) - 4, 8), (1 << 40, 3)):
         table = (ctypes.c_float * (2 * t_count))()
         assert Z.zero_policy_table_fill(hp, t_first, t_count, ctypes.addressof(table)) == Z.ZERO_OK
         for i in range(t_count):
